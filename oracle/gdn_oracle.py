@@ -1,0 +1,213 @@
+"""CPU oracle for the verify step of one Gated DeltaNet (GDN) layer.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import, call or
+execute this module: only ``tests/``, ``__graft_entry__.smoke()`` and the CPU
+baseline / reference arm of ``bench.py`` use it.  It shares no code with the
+CUDA path.
+
+It is the plain definition of the step, computed in float64 one token at a
+time, in the order the pages give it:
+
+  a1  causal conv1d update over the q|k|v channels with its history window and
+      SiLU, writing the history back and keeping one history snapshot per
+      window token  (lucebox #637 "NVLink fix for PR625", commit list:
+      ``ggml_ssm_conv_step`` "history window + silu(conv) + in-place history
+      write-back + optional rollback window copy"; atlas #297, commit "SSM/GDN
+      layer-level pieces of the K=gamma verify path":
+      ``causal_conv1d_update_prefill_inter`` "writes per-token conv_state
+      intermediates for partial-accept rollback")
+  a2  one L2 norm over the q|k slab (lucebox #637, commit list: "single
+      l2_norm over the q|k slab")
+  a3  raw gates beta = sigmoid(b), g = exp(softplus(a + dt_bias) * A) with the
+      softplus clipped to the identity above 20, A = -exp(A_log) (lucebox #637,
+      review of ggml-cuda/gated_delta_net.cu at line 404, "raw-gate mode")
+  a4  gated delta rule per v-head, q/k heads broadcast to the v heads
+      (lucebox #637, commit list: "no q/k head repeat (the kernel
+      broadcasts)"), keeping the state after every window token (atlas #297:
+      ``gated_delta_rule_wy16.cu`` "writing final h_state and Hi_0..Hi_14
+      intermediates in one pass")
+  a5  rollback to the accepted length (strix-llama.cpp #14 "WIP: DSv4 +
+      Qwen3.8 Flash runtime fixes", commits on recurrent snapshot planes and on
+      restoring full checkpoints)
+
+Readings taken where the pages are silent (each is also listed in the design
+notes): taps are a cross-correlation with w[c, W-1] on the current token; no
+conv bias; the L2 norm is x / sqrt(sum x^2 + eps); v-head h reads q/k head
+h // (Hv / Hk); o_t = q_scale * S_t q_t; the state is stored [B, Hv, dv, dk]
+(row = v index); conv snapshot t is the W-1 newest window rows after token t.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against
+closed forms, invariants, special cases and brute force, not against itself.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SOFTPLUS_THRESHOLD = 20.0   # lucebox #637, review of gated_delta_net.cu:404: "(a > 20.0f) ? a : logf(1 + expf(a))"
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """SiLU(z) = z * sigmoid(z)."""
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def conv_step(x: np.ndarray, conv_w: np.ndarray, hist: np.ndarray):
+    """a1: causal conv1d update over a window of K tokens.
+
+    x      [B, K, C]   new inputs (values of the bf16 activations)
+    conv_w [C, W]      taps; w[c, W-1] multiplies the newest row
+    hist   [B, W-1, C] history, oldest row first
+
+    Returns (y [B,K,C], conv_inter [B,K,W-1,C], hist_out [B,W-1,C]) where
+    y_t[c] = SiLU(sum_j w[c,j] * win[t+j][c]) over win = [hist; x],
+    conv_inter[:, t] = the W-1 newest rows of win after token t, and
+    hist_out = conv_inter[:, K-1].
+    """
+    x = np.asarray(x, np.float64)
+    w = np.asarray(conv_w, np.float64)
+    hist = np.asarray(hist, np.float64)
+    B, K, C = x.shape
+    W = w.shape[1]
+    win = np.concatenate([hist, x], axis=1)          # [B, W-1+K, C]
+    y = np.empty((B, K, C))
+    for t in range(K):
+        acc = np.zeros((B, C))
+        for j in range(W):
+            acc += w[:, j] * win[:, t + j, :]
+        y[:, t, :] = silu(acc)
+    conv_inter = np.stack([win[:, t + 1:t + W, :] for t in range(K)], axis=1)
+    hist_out = win[:, K:K + W - 1, :].copy()
+    return y, conv_inter, hist_out
+
+
+def split_qkv(y: np.ndarray, Hk: int, Hv: int, dk: int, dv: int):
+    """Channel order of the conv slab: q | k | v, each head contiguous."""
+    B, K, _ = y.shape
+    q = y[..., :Hk * dk].reshape(B, K, Hk, dk)
+    k = y[..., Hk * dk:2 * Hk * dk].reshape(B, K, Hk, dk)
+    v = y[..., 2 * Hk * dk:2 * Hk * dk + Hv * dv].reshape(B, K, Hv, dv)
+    return q, k, v
+
+
+def l2_normalize(z: np.ndarray, eps: float) -> np.ndarray:
+    """a2: z / sqrt(sum z^2 + eps) over the last axis."""
+    return z / np.sqrt(np.sum(z * z, axis=-1, keepdims=True) + eps)
+
+
+def softplus_clipped(z: np.ndarray) -> np.ndarray:
+    """softplus(z) = log(1 + e^z), replaced by z itself above the threshold 20."""
+    z = np.asarray(z, np.float64)
+    with np.errstate(over="ignore"):
+        return np.where(z > SOFTPLUS_THRESHOLD, z, np.log1p(np.exp(np.minimum(z, SOFTPLUS_THRESHOLD))))
+
+
+def raw_gates(a: np.ndarray, b: np.ndarray, A_log: np.ndarray, dt_bias: np.ndarray):
+    """a3: beta = sigmoid(b); g = exp(softplus(a + dt_bias) * A), A = -exp(A_log).
+
+    a, b [B, K, Hv]; A_log, dt_bias [Hv].  Returns (beta, g), both [B, K, Hv].
+    """
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    with np.errstate(over="ignore"):
+        A = -np.exp(np.asarray(A_log, np.float64))
+        sp = softplus_clipped(a + np.asarray(dt_bias, np.float64))
+        g = np.exp(sp * A)
+        beta = 1.0 / (1.0 + np.exp(-b))
+    return beta, g
+
+
+def delta_rule(qn, kn, v, beta, g, S0, q_scale: float = 1.0):
+    """a4: the gated delta rule, one token after another.
+
+    qn, kn [B, K, Hk, dk]  normalised queries / keys
+    v      [B, K, Hv, dv]
+    beta, g [B, K, Hv]
+    S0     [B, Hv, dv, dk] state before the window (row = v index)
+
+    For every v-head h (reading q/k head h // (Hv/Hk)) and token t:
+        p   = S k_t
+        S  <- g_t S + beta_t (v_t - g_t p) k_t^T
+        o_t = q_scale * S q_t
+    Returns (o [B,K,Hv,dv], states [B,K,Hv,dv,dk]) with states[:, t] the state
+    after token t.
+    """
+    qn = np.asarray(qn, np.float64)
+    kn = np.asarray(kn, np.float64)
+    v = np.asarray(v, np.float64)
+    B, K, Hk, dk = kn.shape
+    Hv, dv = v.shape[2], v.shape[3]
+    r = Hv // Hk
+    kh = np.arange(Hv) // r                          # grouped broadcast of q/k heads
+    S = np.array(S0, dtype=np.float64, copy=True)
+    o = np.empty((B, K, Hv, dv))
+    states = np.empty((B, K, Hv, dv, dk))
+    for t in range(K):
+        k_t = kn[:, t, kh, :]                        # [B, Hv, dk]
+        q_t = qn[:, t, kh, :]
+        g_t = g[:, t, :, None, None]
+        b_t = beta[:, t, :, None]
+        p = np.einsum("bhij,bhj->bhi", S, k_t)       # S k_t
+        delta = b_t * (v[:, t] - g[:, t, :, None] * p)
+        S = g_t * S + delta[..., :, None] * k_t[..., None, :]
+        o[:, t] = q_scale * np.einsum("bhij,bhj->bhi", S, q_t)
+        states[:, t] = S
+    return o, states
+
+
+def verify_step(dims, x, a, b, A_log, dt_bias, conv_w, conv_state, state,
+                q_scale: float = 1.0, l2_eps: float = 1e-6):
+    """a1..a4 over one window of K tokens for B sequences.
+
+    dims: object with Hk, Hv, dk, dv.  Activations are the (bf16) values as
+    floats; conv_state is [B, W-1, C]; state is [B, Hv, dv, dk].
+    Returns a dict with
+      out            [B, K, Hv, dv]
+      states         [B, K, Hv, dv, dk]   state after each token
+      state_out      [B, Hv, dv, dk]      = states[:, K-1]
+      state_inter    [B, K-1, Hv, dv, dk] = states[:, :K-1]
+      conv_inter     [B, K, W-1, C]
+      conv_state_out [B, W-1, C]          = conv_inter[:, K-1]
+      y              [B, K, C]            conv output (after SiLU)
+    """
+    y, conv_inter, hist_out = conv_step(x, conv_w, conv_state)
+    q, k, v = split_qkv(y, dims.Hk, dims.Hv, dims.dk, dims.dv)
+    qn = l2_normalize(q, l2_eps)
+    kn = l2_normalize(k, l2_eps)
+    beta, g = raw_gates(a, b, A_log, dt_bias)
+    o, states = delta_rule(qn, kn, v, beta, g, state, q_scale)
+    return {
+        "out": o,
+        "states": states,
+        "state_out": states[:, -1],
+        "state_inter": states[:, :-1],
+        "conv_inter": conv_inter,
+        "conv_state_out": hist_out,
+        "y": y,
+    }
+
+
+def rollback(accept_len, state0, states, conv_state0, conv_inter):
+    """a5: per sequence, keep the first L tokens of the window.
+
+    accept_len [B] in 0..K; state0 / conv_state0 are the pre-window state and
+    history; states [B,K,...] and conv_inter [B,K,W-1,C] come from verify_step.
+    Returns (state, conv_state) = (S after L tokens, history after L tokens),
+    which for L = 0 is the pre-window state.
+    """
+    accept_len = np.asarray(accept_len)
+    B = accept_len.shape[0]
+    K = states.shape[1]
+    st = np.empty_like(np.asarray(states[:, 0], np.float64))
+    cs = np.empty_like(np.asarray(conv_inter[:, 0], np.float64))
+    for bi in range(B):
+        L = int(accept_len[bi])
+        if not 0 <= L <= K:
+            raise ValueError(f"accept length {L} outside 0..{K}")
+        if L == 0:
+            st[bi] = state0[bi]
+            cs[bi] = conv_state0[bi]
+        else:
+            st[bi] = states[bi, L - 1]
+            cs[bi] = conv_inter[bi, L - 1]
+    return st, cs
