@@ -1,0 +1,152 @@
+/*
+ * gdn.h - C ABI of the GB300 (sm_103a) speculative-decoding verify step of one
+ * Gated DeltaNet (GDN) linear-attention layer.
+ *
+ * For B sequences and a window of K tokens (the seed token plus K-1 drafted
+ * tokens) the step is
+ *   a1  causal conv1d update over the q|k|v channels with its history window
+ *       and SiLU, writing the history back and one history snapshot per token
+ *       (lucebox #637 "NVLink fix for PR625", commit list: ggml_ssm_conv_step;
+ *       atlas #297 "verify-step glue", commit on SSM/GDN verify kernels:
+ *       causal_conv1d_update_prefill_inter),
+ *   a2  one L2 norm over the q|k slab (lucebox #637, commit list),
+ *   a3  raw gates beta = sigmoid(b), g = exp(softplus(a + dt_bias) * A) with
+ *       A = -exp(A_log) and softplus clipped to the identity above 20
+ *       (lucebox #637, review of ggml-cuda/gated_delta_net.cu line 404),
+ *   a4  the gated delta rule S_t = g_t S_{t-1} + beta_t (v_t - g_t S_{t-1} k_t) k_t^T,
+ *       o_t = q_scale * S_t q_t, q/k heads broadcast to the v heads
+ *       (v-head h reads q/k head h / (Hv/Hk)), writing the final state and the
+ *       K-1 intermediate states in one pass (atlas #297: gated_delta_rule_wy16.cu),
+ *   a5  rollback of state and conv history to each sequence's accepted length
+ *       (strix-llama.cpp #14 "WIP: DSv4 + Qwen3.8 Flash runtime fixes", commits
+ *       on recurrent snapshot rollback and device checkpoints).
+ *
+ * Conventions common to every call
+ *  - Layouts are row-major with the last index fastest (shapes below).
+ *  - Ownership: the caller owns every buffer.  The library allocates and frees
+ *    nothing; its only state is a thread-local error message and one 32-bit
+ *    device status word per GPU (see gdn_device_status).
+ *  - Asynchrony: calls validate on the host, enqueue kernels on `stream` and
+ *    return; launch failures come back as GDN_ERR_CUDA.
+ *  - Validation happens before any launch: a non-OK status means nothing was
+ *    enqueued.  No call aborts the process.
+ *  - Supported shapes: 1 <= K <= 16, dk and dv in {64, 128}, Hk >= 1,
+ *    Hv % Hk == 0, Hv / Hk <= 16, conv width W == 4, B >= 0 (B == 0 is a
+ *    no-op), channels C = 2*Hk*dk + Hv*dv.
+ *  - Alignment: every float / bf16 buffer must be 16-byte aligned.
+ */
+#ifndef GDN_GB300_H
+#define GDN_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (the same object as cudaStream_t / CUstream). NULL = legacy default stream. */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1, /* null pointer, bad size, misalignment, non-finite scalar */
+  GDN_ERR_UNSUPPORTED = 2, /* shape outside the supported set above */
+  GDN_ERR_ALIAS = 3,       /* buffers overlap where the call forbids it */
+  GDN_ERR_NO_SNAPSHOT = 4, /* rollback asked for a snapshot that was not passed */
+  GDN_ERR_CUDA = 5         /* a CUDA runtime call failed (message in gdn_last_error) */
+} gdn_status;
+
+/* Bits of the per-device status word (set by kernels, read by gdn_device_status). */
+#define GDN_DEVERR_TIMEOUT 1u      /* a bounded wait in a kernel gave up; its results are invalid */
+#define GDN_DEVERR_ACCEPT_RANGE 2u /* rollback saw an accept length outside 0..K; that sequence was left as is */
+#define GDN_DEVERR_NO_SNAPSHOT 4u  /* rollback saw accept length 0 with no snapshot; that sequence was left as is */
+
+typedef struct {
+  int32_t B;       /* sequences */
+  int32_t K;       /* window tokens: seed + drafts, 1..16 */
+  int32_t Hk;      /* q/k heads */
+  int32_t Hv;      /* v heads (a multiple of Hk) */
+  int32_t dk;      /* q/k head dim, 64 or 128 */
+  int32_t dv;      /* v head dim, 64 or 128 */
+  int32_t conv_w;  /* conv taps W, must be 4 */
+  float q_scale;   /* o_t = q_scale * S_t q_t (1.0 for the plain rule) */
+  float l2_eps;    /* L2 norm: z / sqrt(sum z^2 + l2_eps), >= 0 */
+  int32_t out_f32; /* 0: outputs in bf16, 1: outputs in f32 */
+} gdn_dims;
+
+/*
+ * a1 alone: causal conv1d update with SiLU (lucebox #637 commit list,
+ * ggml_ssm_conv_step: history window + silu(conv) + in-place history
+ * write-back + rollback window copy).
+ *   x          [B, K, C]       bf16 (uint16 bit patterns), channel fastest
+ *   conv_w     [C, W]          f32; w[c][W-1] multiplies the newest row
+ *   conv_state [B, W-1, C]     f32, oldest row first; read, then overwritten
+ *                              in place with the history after token K-1
+ *   conv_inter [B, K, W-1, C]  f32 or NULL; snapshot t = the W-1 newest
+ *                              window rows after token t
+ *   y          [B, K, C]       f32 if out_f32 else bf16: SiLU(conv) per token
+ * No bias.  conv_inter and y must not overlap each other or the inputs.
+ */
+gdn_status gdn_conv_step(const gdn_dims* dims, const uint16_t* x, const float* conv_w, float* conv_state,
+                         float* conv_inter, void* y, gdn_stream_t stream);
+
+/*
+ * a1..a4 fused: one verify window for B sequences.
+ *   x               [B, K, C]         bf16; channel order q | k | v, each head contiguous
+ *   a, b            [B, K, Hv]        bf16 raw gate inputs (alpha, beta projections)
+ *   A_log, dt_bias  [Hv]              f32
+ *   conv_w          [C, W]            f32
+ *   conv_state_in   [B, W-1, C]       f32 history before the window
+ *   conv_state_out  [B, W-1, C]       f32 history after token K-1; may equal
+ *                                     conv_state_in (in place), else no overlap
+ *   conv_inter      [B, K, W-1, C]    f32 or NULL: history after each token
+ *   state_in        [B, Hv, dv, dk]   f32 state before the window (row = v index)
+ *   state_out       [B, Hv, dv, dk]   f32 state after token K-1; may equal
+ *                                     state_in (in place), else no overlap
+ *   state_inter     [B, K-1, Hv, dv, dk] f32: state after tokens 0..K-2;
+ *                                     NULL allowed only when K == 1
+ *   out             [B, K, Hv, dv]    bf16 or f32 (out_f32): o_t = q_scale * S_t q_t
+ * Intermediates and out must not overlap any other buffer.
+ */
+gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16_t* a, const uint16_t* b,
+                           const float* A_log, const float* dt_bias, const float* conv_w,
+                           const float* conv_state_in, float* conv_state_out, float* conv_inter,
+                           const float* state_in, float* state_out, float* state_inter, void* out,
+                           gdn_stream_t stream);
+
+/*
+ * a5: per sequence, keep the first L = accept_len[b] window tokens
+ * (strix-llama.cpp #14: snapshot restore of the recurrent state; lucebox #637:
+ * rollback window copy of the conv history).
+ *   accept_len_dev          [B] int32 on the device, each in 0..K
+ *   state_in_snapshot       [B, Hv, dv, dk] f32 or NULL: the state before the
+ *                           window (needed only for L == 0; must not overlap state)
+ *   state                   [B, Hv, dv, dk] f32, holds the state after token K-1
+ *                           on entry (verify's state_out) and S_L on exit
+ *   state_inter             [B, K-1, Hv, dv, dk] f32 from gdn_verify_step (NULL iff K == 1)
+ *   conv_state_in_snapshot  [B, W-1, C] f32 or NULL (for L == 0; no overlap with conv_state)
+ *   conv_state              [B, W-1, C] f32, history after token K-1 on entry, after L tokens on exit
+ *   conv_inter              [B, K, W-1, C] f32 from gdn_verify_step (NULL iff K == 1)
+ * L == K leaves a sequence untouched.  Lengths are read on the device: an
+ * out-of-range length, or L == 0 with no snapshot, leaves that sequence
+ * untouched and sets a bit in the device status word.
+ */
+gdn_status gdn_rollback(const gdn_dims* dims, const int32_t* accept_len_dev, const float* state_in_snapshot,
+                        float* state, const float* state_inter, const float* conv_state_in_snapshot,
+                        float* conv_state, const float* conv_inter, gdn_stream_t stream);
+
+/*
+ * Reads (and, if clear != 0, resets) the current device's status word after
+ * synchronising `stream`.  *flags receives the OR of GDN_DEVERR_* bits set by
+ * kernels since the last clear.
+ */
+gdn_status gdn_device_status(uint32_t* flags, int32_t clear, gdn_stream_t stream);
+
+/* Message of the last non-OK status returned on this thread ("" if none). */
+const char* gdn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_GB300_H */

@@ -1,0 +1,158 @@
+"""Host side of the C ABI: the library loads, exports every declared entry point, and
+rejects bad arguments before anything is enqueued.
+
+Every call here with made-up pointers is built to fail validation (bad shape, NULL,
+misalignment or overlap), which happens before the library touches CUDA, so these tests
+run without a GPU and never launch a kernel.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decode_verify_gdn_gb300 import gdn
+from speculative_decode_verify_gdn_gb300.build import LIB_PATH, build_library
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_library()
+    return gdn.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(gdn_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert set(names) == set(gdn.EXPORTED)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+BASE = dict(B=2, K=4, Hk=2, Hv=4, dk=64, dv=64)
+P = 1 << 32          # fake, never dereferenced: every call below fails validation first
+MB = 1 << 24
+
+
+def _ptrs(n, step=MB):
+    return [ctypes.c_void_p(P + i * step) for i in range(n)]
+
+
+def _verify(lib, dims, ptrs):
+    return lib.gdn_verify_step(ctypes.byref(dims), *ptrs, None)
+
+
+def test_last_error_and_bad_dims(lib):
+    assert lib.gdn_verify_step(None, *_ptrs(13), None) == gdn.GDN_ERR_INVALID_ARG
+    assert "dims" in gdn.last_error()
+    cases = [
+        (dict(K=0), gdn.GDN_ERR_UNSUPPORTED), (dict(K=17), gdn.GDN_ERR_UNSUPPORTED),
+        (dict(dk=96), gdn.GDN_ERR_UNSUPPORTED), (dict(dv=256), gdn.GDN_ERR_UNSUPPORTED),
+        (dict(Hv=5), gdn.GDN_ERR_UNSUPPORTED), (dict(Hk=0), gdn.GDN_ERR_INVALID_ARG),
+        (dict(B=-1), gdn.GDN_ERR_INVALID_ARG), (dict(W=3), gdn.GDN_ERR_UNSUPPORTED),
+        (dict(out_f32=2), gdn.GDN_ERR_INVALID_ARG), (dict(l2_eps=-1.0), gdn.GDN_ERR_INVALID_ARG),
+        (dict(q_scale=float("nan")), gdn.GDN_ERR_INVALID_ARG),
+        (dict(Hk=1, Hv=32, dv=128), gdn.GDN_ERR_UNSUPPORTED),   # 32 v-heads per q/k head
+    ]
+    for over, status in cases:
+        kw = dict(BASE)
+        kw.update(over)
+        dims = gdn.make_dims(**kw)
+        assert _verify(lib, dims, _ptrs(13)) == status, over
+        assert gdn.last_error() != ""
+
+
+def test_empty_batch_is_a_noop(lib):
+    dims = gdn.make_dims(**dict(BASE, B=0))
+    assert _verify(lib, dims, [None] * 13) == gdn.GDN_OK
+    assert gdn.last_error() == ""
+    assert lib.gdn_conv_step(ctypes.byref(dims), None, None, None, None, None, None) == gdn.GDN_OK
+    assert lib.gdn_rollback(ctypes.byref(dims), None, None, None, None, None, None, None, None) == gdn.GDN_OK
+
+
+def test_null_and_misaligned_pointers(lib):
+    dims = gdn.make_dims(**BASE)
+    for i in range(13):
+        if i in (8,):          # conv_inter is optional
+            continue
+        ptrs = _ptrs(13)
+        ptrs[i] = None
+        assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_INVALID_ARG, i
+        ptrs = _ptrs(13)
+        ptrs[i] = ctypes.c_void_p(P + i * MB + 4)
+        assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_INVALID_ARG, i
+        assert "aligned" in gdn.last_error()
+
+
+def test_aliasing_rules(lib):
+    dims = gdn.make_dims(**BASE)
+    # out overlapping x
+    ptrs = _ptrs(13)
+    ptrs[12] = ptrs[0]
+    assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_ALIAS
+    # state_out partially overlapping state_in (shifted by 16 bytes)
+    ptrs = _ptrs(13)
+    ptrs[10] = ctypes.c_void_p(ptrs[9].value + 16)
+    assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_ALIAS
+    # state_inter overlapping state_out
+    ptrs = _ptrs(13)
+    ptrs[11] = ctypes.c_void_p(ptrs[10].value + 64)
+    assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_ALIAS
+    # conv_inter overlapping conv_state_in
+    ptrs = _ptrs(13)
+    ptrs[8] = ptrs[6]
+    assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_ALIAS
+    # K > 1 needs state_inter
+    ptrs = _ptrs(13)
+    ptrs[11] = None
+    assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_rollback_validation(lib):
+    dims = gdn.make_dims(**BASE)
+    pt = _ptrs(7)   # accept_len, state_snap, state, state_inter, conv_snap, conv_state, conv_inter
+    # only one of the two snapshots
+    args = list(pt)
+    args[4] = None
+    assert lib.gdn_rollback(ctypes.byref(dims), *args, None) == gdn.GDN_ERR_NO_SNAPSHOT
+    # state overlapping state_inter
+    args = list(pt)
+    args[2] = args[3]
+    assert lib.gdn_rollback(ctypes.byref(dims), *args, None) == gdn.GDN_ERR_ALIAS
+    # K > 1 without intermediates
+    args = list(pt)
+    args[3] = None
+    assert lib.gdn_rollback(ctypes.byref(dims), *args, None) == gdn.GDN_ERR_INVALID_ARG
+    args = list(pt)
+    args[0] = ctypes.c_void_p(P + 2)
+    assert lib.gdn_rollback(ctypes.byref(dims), *args, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_conv_step_validation(lib):
+    dims = gdn.make_dims(**BASE)
+    pt = _ptrs(5)
+    args = list(pt)
+    args[4] = args[0]                    # y overlapping x
+    assert lib.gdn_conv_step(ctypes.byref(dims), *args, None) == gdn.GDN_ERR_ALIAS
+    args = list(pt)
+    args[2] = None
+    assert lib.gdn_conv_step(ctypes.byref(dims), *args, None) == gdn.GDN_ERR_INVALID_ARG
+
+
+def test_binding_refuses_cpu_tensors():
+    import torch
+    dims = gdn.make_dims(**BASE)
+    t = torch.zeros(4)
+    with pytest.raises(ValueError):
+        gdn.gdn_conv_step(dims, t, t, t, None, t)
+
+
+def test_library_path_in_tree():
+    assert os.path.dirname(LIB_PATH).endswith("speculative_decode_verify_gdn_gb300")
