@@ -41,6 +41,7 @@ WORKLOAD = "serve16"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 129 * 1024 * 1024
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gdn_verify_kernel_serve16.md")
+LAUNCHES_PER_STEP = 3   # q/k prologue, state stream, rollback
 
 
 # ------------------------------------------------------------------ algorithmic bytes
@@ -175,6 +176,22 @@ def cpu_oracle_throughput(seconds: float = 12.0, n_tok: int = 16):
     return rounds * n_tok / wall, procs, rounds, wall
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of each rank's `x` (the slowest rank sets the job's time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ device arm
 def run_gdn(args):
     import torch
@@ -217,14 +234,14 @@ def run_gdn(args):
     accs = [torch.from_numpy(r.accept_len).to(dev) for r in rnds]
     stream = torch.cuda.current_stream()
     dims = st.dims
-    S0, CS, CI, SI, OUT = st.states[0], st.conv_states[0], st.conv_inter, st.state_inter, st.out
+    S0, CS, CI, SI, OUT, WS = st.states[0], st.conv_states[0], st.conv_inter, st.state_inter, st.out, st.workspace
 
     def step(i, ev=None):
         j = i % n_in
         if ev is not None:
             ev[0].record(stream)
         gdn.gdn_verify_step(dims, xs[j], as_[j], bs[j], st.A_log, st.dt_bias, st.conv_w, CS, CS, CI, S0, S0, SI,
-                            OUT, stream)
+                            OUT, WS, stream)
         if ev is not None:
             ev[1].record(stream)
         gdn.gdn_rollback(dims, accs[j], None, S0, SI, None, CS, CI, stream)
@@ -250,12 +267,8 @@ def run_gdn(args):
     flags = gdn.gdn_device_status(clear=True)
     if flags:
         raise RuntimeError(f"device status flags {flags} after the timed steps")
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens = world * d.B * d.K * args.steps
-    value = tokens / (ms / 1e3)
+    ms = max_over_ranks(ms, world, dev)
+    value = job_throughput(d.B * d.K * args.steps, world, ms)
 
     # e2e: inputs from pinned host memory and the output back, inside the timed region
     e2e = None
@@ -273,7 +286,7 @@ def run_gdn(args):
             A.copy_(ha[j], non_blocking=True)
             Bq.copy_(hb[j], non_blocking=True)
             ACC.copy_(hacc[j], non_blocking=True)
-            gdn.gdn_verify_step(dims, X, A, Bq, st.A_log, st.dt_bias, st.conv_w, CS, CS, CI, S0, S0, SI, OUT,
+            gdn.gdn_verify_step(dims, X, A, Bq, st.A_log, st.dt_bias, st.conv_w, CS, CS, CI, S0, S0, SI, OUT, WS,
                                 stream)
             gdn.gdn_rollback(dims, ACC, None, S0, SI, None, CS, CI, stream)
             hout.copy_(OUT, non_blocking=True)
@@ -288,14 +301,10 @@ def run_gdn(args):
             e2e_step(i)
         e1.record(stream)
         barrier()
-        ems = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([ems], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
         bi = sum(t.numel() * t.element_size() for t in (hx[0], ha[0], hb[0], hacc[0]))
         bo = hout.numel() * hout.element_size()
-        e2e = {"value": world * d.B * d.K * n_e2e / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
+        e2e = {"value": job_throughput(d.B * d.K * n_e2e, world, ems), "unit": UNIT, "h2d_bytes_per_step": bi,
                "d2h_bytes_per_step": bo, "steps": n_e2e}
 
     peak, peak_kind = measured_peak_gbs()
@@ -312,14 +321,15 @@ def run_gdn(args):
                    "global_batch": world * d.B, "seq_len": d.K, "parallelism": f"replicas x{world} (no exchange)",
                    "l2": "no flush: each step moves 1.2 GB (> 129 MB L2)", "per_step": "gdn_verify_step + gdn_rollback"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": profile_traffic(digest), "kernel": "gdn_verify_kernel",
+                     "traffic": profile_traffic(digest),
+                     "kernel": "gdn_verify_step (gdn_qk_prologue_kernel + gdn_state_stream_kernel, overlapped)",
                      "algorithmic_bytes_per_launch": vbytes, "launch_ms": verify_ms,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "kernel_digest": digest},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks.summary(),
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
     }
     if world > 1:
         dist.barrier()

@@ -23,16 +23,16 @@
  *
  * Conventions common to every call
  *  - Layouts are row-major with the last index fastest (shapes below).
- *  - Ownership: the caller owns every buffer.  The library allocates and frees
- *    nothing; its only state is a thread-local error message and one 32-bit
- *    device status word per GPU (see gdn_device_status).
+ *  - Ownership: the caller owns every buffer, scratch included.  The library
+ *    allocates and frees nothing; its only state is a thread-local error
+ *    message and one 32-bit device status word per GPU (see gdn_device_status).
  *  - Asynchrony: calls validate on the host, enqueue kernels on `stream` and
  *    return; launch failures come back as GDN_ERR_CUDA.
  *  - Validation happens before any launch: a non-OK status means nothing was
  *    enqueued.  No call aborts the process.
  *  - Supported shapes: 1 <= K <= 16, dk and dv in {64, 128}, Hk >= 1,
- *    Hv % Hk == 0, Hv / Hk <= 16, conv width W == 4, B >= 0 (B == 0 is a
- *    no-op), channels C = 2*Hk*dk + Hv*dv.
+ *    Hv % Hk == 0, conv width W == 4, 0 <= B <= 65535 (B == 0 is a no-op),
+ *    channels C = 2*Hk*dk + Hv*dv.
  *  - Alignment: every float / bf16 buffer must be 16-byte aligned.
  */
 #ifndef GDN_GB300_H
@@ -106,13 +106,27 @@ gdn_status gdn_conv_step(const gdn_dims* dims, const uint16_t* x, const float* c
  *   state_inter     [B, K-1, Hv, dv, dk] f32: state after tokens 0..K-2;
  *                                     NULL allowed only when K == 1
  *   out             [B, K, Hv, dv]    bf16 or f32 (out_f32): o_t = q_scale * S_t q_t
- * Intermediates and out must not overlap any other buffer.
+ *   workspace       device scratch of at least gdn_verify_workspace_size() bytes,
+ *                   16-byte aligned; holds the normalised q/k, Gram products and
+ *                   gates that pass from the q/k prologue kernel to the state
+ *                   kernel.  Contents need no initialisation and are dead after the
+ *                   call; calls that overlap on the GPU must not share it.
+ * Intermediates, out and workspace must not overlap any other buffer.
+ * Runs as two kernels on `stream`: a per-(sequence, q/k head) prologue and a
+ * per-(sequence, v-head, 32-row tile) state kernel started with programmatic
+ * dependent launch.
  */
 gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16_t* a, const uint16_t* b,
                            const float* A_log, const float* dt_bias, const float* conv_w,
                            const float* conv_state_in, float* conv_state_out, float* conv_inter,
                            const float* state_in, float* state_out, float* state_inter, void* out,
-                           gdn_stream_t stream);
+                           void* workspace, uint64_t workspace_bytes, gdn_stream_t stream);
+
+/*
+ * Bytes of workspace gdn_verify_step needs for `dims`:
+ * 4 * (B*Hk*(32*dk + 16*dk) + B*Hv*596).  Validates dims like gdn_verify_step.
+ */
+gdn_status gdn_verify_workspace_size(const gdn_dims* dims, uint64_t* bytes);
 
 /*
  * a5: per sequence, keep the first L = accept_len[b] window tokens

@@ -84,8 +84,6 @@ gdn_status check_dims(const gdn_dims* d, bool need_gates) {
   if (need_gates) {
     if (!std::isfinite(d->q_scale)) return fail(GDN_ERR_INVALID_ARG, "q_scale not finite");
     if (!std::isfinite(d->l2_eps) || d->l2_eps < 0.f) return fail(GDN_ERR_INVALID_ARG, "l2_eps must be finite, >= 0");
-    if (gdn::verify_cluster_size(d->dv, d->Hv / d->Hk) == 0)
-      return fail(GDN_ERR_UNSUPPORTED, "Hv/Hk=%d too large for dv=%d", d->Hv / d->Hk, d->dv);
   }
   return GDN_OK;
 }
@@ -150,11 +148,19 @@ gdn_status gdn_conv_step(const gdn_dims* dims, const uint16_t* x, const float* c
   return ok();
 }
 
+gdn_status gdn_verify_workspace_size(const gdn_dims* dims, uint64_t* bytes) {
+  gdn_status s = check_dims(dims, true);
+  if (s != GDN_OK) return s;
+  if (!bytes) return fail(GDN_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = gdn::workspace_bytes(dims->B, dims->Hk, dims->Hv, dims->dk);
+  return ok();
+}
+
 gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16_t* a, const uint16_t* b,
                            const float* A_log, const float* dt_bias, const float* conv_w,
                            const float* conv_state_in, float* conv_state_out, float* conv_inter,
                            const float* state_in, float* state_out, float* state_inter, void* out,
-                           gdn_stream_t stream) {
+                           void* workspace, uint64_t workspace_bytes, gdn_stream_t stream) {
   gdn_status s = check_dims(dims, true);
   if (s != GDN_OK) return s;
   const gdn_dims& d = *dims;
@@ -172,7 +178,11 @@ gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16
   GDN_CHECK_PTR(state_out, "state_out");
   GDN_CHECK_OPT_PTR(state_inter, "state_inter");
   GDN_CHECK_PTR(out, "out");
+  GDN_CHECK_PTR(workspace, "workspace");
   if (d.K > 1 && !state_inter) return fail(GDN_ERR_INVALID_ARG, "state_inter is NULL with K=%d > 1", d.K);
+  const size_t ws_need = gdn::workspace_bytes(d.B, d.Hk, d.Hv, d.dk);
+  if (workspace_bytes < ws_need)
+    return fail(GDN_ERR_INVALID_ARG, "workspace has %llu bytes, needs %zu", (unsigned long long)workspace_bytes, ws_need);
 
   const size_t C = 2ull * d.Hk * d.dk + size_t(d.Hv) * d.dv;
   const size_t B = size_t(d.B), K = size_t(d.K);
@@ -184,22 +194,22 @@ gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16
               r_ci = range_of(conv_inter, B * K * 3 * C * 4), r_si = range_of(state_in, B * S * 4),
               r_so = range_of(state_out, B * S * 4),
               r_sx = range_of(d.K > 1 ? state_inter : nullptr, B * (K - 1) * S * 4),
-              r_o = range_of(out, B * K * d.Hv * d.dv * (d.out_f32 ? 4 : 2));
+              r_o = range_of(out, B * K * d.Hv * d.dv * (d.out_f32 ? 4 : 2)), r_ws = range_of(workspace, ws_need);
   // in-place pairs: identical start or disjoint
   if (conv_state_out != conv_state_in && overlap(r_cso, r_csi))
     return fail(GDN_ERR_ALIAS, "conv_state_out partially overlaps conv_state_in");
   if (state_out != state_in && overlap(r_so, r_si))
     return fail(GDN_ERR_ALIAS, "state_out partially overlaps state_in");
   const Range ins[7] = {r_x, r_a, r_b, r_alog, r_dt, r_w, r_csi};
-  const Range writes[5] = {r_cso, r_ci, r_so, r_sx, r_o};
-  const char* wname[5] = {"conv_state_out", "conv_inter", "state_out", "state_inter", "out"};
-  for (int i = 0; i < 5; ++i) {
+  const Range writes[6] = {r_cso, r_ci, r_so, r_sx, r_o, r_ws};
+  const char* wname[6] = {"conv_state_out", "conv_inter", "state_out", "state_inter", "out", "workspace"};
+  for (int i = 0; i < 6; ++i) {
     for (int j = 0; j < 7; ++j) {
       if (i == 0 && j == 6) continue;  // conv_state_out vs conv_state_in handled above
       if (overlap(writes[i], ins[j])) return fail(GDN_ERR_ALIAS, "%s overlaps an input", wname[i]);
     }
     if (i != 2 && overlap(writes[i], r_si)) return fail(GDN_ERR_ALIAS, "%s overlaps state_in", wname[i]);
-    for (int j = i + 1; j < 5; ++j)
+    for (int j = i + 1; j < 6; ++j)
       if (overlap(writes[i], writes[j])) return fail(GDN_ERR_ALIAS, "%s overlaps %s", wname[i], wname[j]);
   }
 
@@ -220,6 +230,7 @@ gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16
   p.state_out = state_out;
   p.state_inter = d.K > 1 ? state_inter : nullptr;
   p.out = out;
+  p.ws = gdn::workspace_carve(workspace, d.B, d.Hk, d.Hv, d.dk);
   p.err = err;
   p.B = d.B;
   p.K = d.K;

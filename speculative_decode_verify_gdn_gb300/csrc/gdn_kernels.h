@@ -9,6 +9,28 @@ namespace gdn {
 
 constexpr int kKMax = 16;  // longest verify window a launch handles
 constexpr int kConvW = 4;  // conv taps
+constexpr int kNCol = 2 * kKMax;  // columns of the normalised q/k table: k^ in [0,16), q^ in [16,32)
+constexpr int kMStride = kKMax + 1;
+// Per-(sequence, v-head) gate block: M[16][17], N[16][17], beta[16], g[16], Gamma[16], padding.
+constexpr int kGateFloats = 2 * kKMax * kMStride + 3 * kKMax + 4;  // 596 floats = 2384 bytes (16-byte multiple)
+constexpr int kGateOffN = kKMax * kMStride;
+constexpr int kGateOffBeta = 2 * kKMax * kMStride;
+constexpr int kGateOffG = kGateOffBeta + kKMax;
+constexpr int kGateOffGam = kGateOffG + kKMax;
+
+// Workspace written by the q/k prologue kernel and read by the state kernel:
+//   wt   [B][Hk][dk][32]   normalised k^ (columns 0..15) and q^ (16..31), column index
+//                          swizzled as col ^ (c & 31) so both kernels access it conflict-free
+//   kn   [B][Hk][16][dk]   normalised k^, token-major
+//   gate [B][Hv][kGateFloats]
+struct Workspace {
+  float* wt;
+  float* kn;
+  float* gate;
+};
+
+size_t workspace_bytes(int B, int Hk, int Hv, int dk);
+Workspace workspace_carve(void* base, int B, int Hk, int Hv, int dk);
 
 struct VerifyParams {
   const uint16_t* x;
@@ -24,6 +46,7 @@ struct VerifyParams {
   float* state_out;
   float* state_inter;  // null only when K == 1
   void* out;
+  Workspace ws;
   uint32_t* err;       // device status word
   int B, K, Hk, Hv, dk, dv, C;
   float q_scale, l2_eps;
@@ -53,12 +76,6 @@ struct RollbackParams {
   long long state_elems;  // per sequence: Hv*dv*dk
   long long conv_elems;   // per sequence: (W-1)*C
 };
-
-// Row tile of one v-head's state handled by one CTA of the verify kernel, for these dims.
-int verify_row_tile(int dv, int r);
-// Cluster size of the verify kernel (CTAs sharing one q/k head), 0 if unsupported.
-int verify_cluster_size(int dv, int r);
-size_t verify_smem_bytes(int dk, int dv, int r);
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t stream);

@@ -14,7 +14,8 @@ import torch
 
 from .build import LIB_PATH
 
-EXPORTED = ("gdn_conv_step", "gdn_verify_step", "gdn_rollback", "gdn_device_status", "gdn_last_error")
+EXPORTED = ("gdn_conv_step", "gdn_verify_step", "gdn_verify_workspace_size", "gdn_rollback", "gdn_device_status",
+            "gdn_last_error")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIAS, GDN_ERR_NO_SNAPSHOT, GDN_ERR_CUDA = range(6)
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIAS",
@@ -57,12 +58,13 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     P = ctypes.c_void_p
     D = ctypes.POINTER(GdnDims)
     lib.gdn_conv_step.argtypes = [D, P, P, P, P, P, P]
-    lib.gdn_verify_step.argtypes = [D] + [P] * 14
+    lib.gdn_verify_step.argtypes = [D] + [P] * 14 + [ctypes.c_uint64, P]
+    lib.gdn_verify_workspace_size.argtypes = [D, ctypes.POINTER(ctypes.c_uint64)]
     lib.gdn_rollback.argtypes = [D] + [P] * 8
     lib.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32, P]
     lib.gdn_last_error.argtypes = []
     lib.gdn_last_error.restype = ctypes.c_char_p
-    for f in ("gdn_conv_step", "gdn_verify_step", "gdn_rollback", "gdn_device_status"):
+    for f in ("gdn_conv_step", "gdn_verify_step", "gdn_verify_workspace_size", "gdn_rollback", "gdn_device_status"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -112,8 +114,20 @@ def gdn_conv_step(dims: GdnDims, x, conv_w, conv_state, conv_inter, y, stream=No
         _ptr(y, "y", ydt, BK * C), _stream(stream)))
 
 
+def gdn_verify_workspace_size(dims: GdnDims) -> int:
+    """Bytes of device scratch gdn_verify_step needs for these dims."""
+    n = ctypes.c_uint64(0)
+    _check(load_library().gdn_verify_workspace_size(ctypes.byref(dims), ctypes.byref(n)))
+    return n.value
+
+
+def alloc_workspace(dims: GdnDims, device="cuda") -> torch.Tensor:
+    """A uint8 device tensor large enough to serve as gdn_verify_step's workspace."""
+    return torch.empty(max(16, gdn_verify_workspace_size(dims)), dtype=torch.uint8, device=device)
+
+
 def gdn_verify_step(dims: GdnDims, x, a, b, A_log, dt_bias, conv_w, conv_state_in, conv_state_out, conv_inter,
-                    state_in, state_out, state_inter, out, stream=None) -> None:
+                    state_in, state_out, state_inter, out, workspace, stream=None) -> None:
     """a1..a4 fused over one verify window (see include/gdn.h for layouts and aliasing)."""
     d = dims
     C, BK = d.C, d.B * d.K
@@ -128,7 +142,20 @@ def gdn_verify_step(dims: GdnDims, x, a, b, A_log, dt_bias, conv_w, conv_state_i
         _ptr(conv_inter, "conv_inter", torch.float32, BK * (d.conv_w - 1) * C, allow_none=True),
         _ptr(state_in, "state_in", torch.float32, d.B * S), _ptr(state_out, "state_out", torch.float32, d.B * S),
         _ptr(state_inter, "state_inter", torch.float32, d.B * (d.K - 1) * S, allow_none=(d.K == 1)),
-        _ptr(out, "out", odt, BK * d.Hv * d.dv), _stream(stream)))
+        _ptr(out, "out", odt, BK * d.Hv * d.dv), _ws_ptr(workspace), ctypes.c_uint64(_ws_bytes(workspace)),
+        _stream(stream)))
+
+
+def _ws_ptr(ws):
+    if ws is None:
+        return None
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda or not ws.is_contiguous():
+        raise ValueError("workspace must be a contiguous CUDA tensor")
+    return ctypes.c_void_p(ws.data_ptr())
+
+
+def _ws_bytes(ws) -> int:
+    return 0 if ws is None else ws.numel() * ws.element_size()
 
 
 def gdn_rollback(dims: GdnDims, accept_len, state_in_snapshot, state, state_inter, conv_state_in_snapshot,

@@ -44,6 +44,7 @@ class GdnLayerState:
     b: torch.Tensor
     out: torch.Tensor          # [B, K, Hv, dv]
     accept_len: torch.Tensor   # [B] int32
+    workspace: torch.Tensor    # scratch of gdn_verify_step
     cur: int = 0
 
     @property
@@ -78,6 +79,7 @@ class GdnLayerState:
             out=torch.empty((d.B, d.K, d.Hv, d.dv), dtype=torch.float32 if out_f32 else torch.bfloat16,
                             device=device),
             accept_len=torch.full((d.B,), d.K, dtype=torch.int32, device=device),
+            workspace=gdn.alloc_workspace(dims, device),
         )
 
     def load_round(self, rnd: Round) -> None:
@@ -91,7 +93,7 @@ class GdnLayerState:
         i, o = (self.cur, 1 - self.cur) if self.keep_snapshot else (0, 0)
         gdn.gdn_verify_step(self.dims, self.x, self.a, self.b, self.A_log, self.dt_bias, self.conv_w,
                             self.conv_states[i], self.conv_states[o], self.conv_inter, self.states[i],
-                            self.states[o], self.state_inter, self.out, stream)
+                            self.states[o], self.state_inter, self.out, self.workspace, stream)
 
     def rollback(self, stream=None) -> None:
         if self.keep_snapshot:

@@ -45,12 +45,15 @@ def _ptrs(n, step=MB):
     return [ctypes.c_void_p(P + i * step) for i in range(n)]
 
 
-def _verify(lib, dims, ptrs):
-    return lib.gdn_verify_step(ctypes.byref(dims), *ptrs, None)
+NV = 14              # pointer arguments of gdn_verify_step (the 14th is the workspace)
+
+
+def _verify(lib, dims, ptrs, ws_bytes=1 << 40):
+    return lib.gdn_verify_step(ctypes.byref(dims), *ptrs, ctypes.c_uint64(ws_bytes), None)
 
 
 def test_last_error_and_bad_dims(lib):
-    assert lib.gdn_verify_step(None, *_ptrs(13), None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_step(None, *_ptrs(NV), ctypes.c_uint64(1 << 40), None) == gdn.GDN_ERR_INVALID_ARG
     assert "dims" in gdn.last_error()
     cases = [
         (dict(K=0), gdn.GDN_ERR_UNSUPPORTED), (dict(K=17), gdn.GDN_ERR_UNSUPPORTED),
@@ -59,19 +62,18 @@ def test_last_error_and_bad_dims(lib):
         (dict(B=-1), gdn.GDN_ERR_INVALID_ARG), (dict(W=3), gdn.GDN_ERR_UNSUPPORTED),
         (dict(out_f32=2), gdn.GDN_ERR_INVALID_ARG), (dict(l2_eps=-1.0), gdn.GDN_ERR_INVALID_ARG),
         (dict(q_scale=float("nan")), gdn.GDN_ERR_INVALID_ARG),
-        (dict(Hk=1, Hv=32, dv=128), gdn.GDN_ERR_UNSUPPORTED),   # 32 v-heads per q/k head
     ]
     for over, status in cases:
         kw = dict(BASE)
         kw.update(over)
         dims = gdn.make_dims(**kw)
-        assert _verify(lib, dims, _ptrs(13)) == status, over
+        assert _verify(lib, dims, _ptrs(NV)) == status, over
         assert gdn.last_error() != ""
 
 
 def test_empty_batch_is_a_noop(lib):
     dims = gdn.make_dims(**dict(BASE, B=0))
-    assert _verify(lib, dims, [None] * 13) == gdn.GDN_OK
+    assert _verify(lib, dims, [None] * NV) == gdn.GDN_OK
     assert gdn.last_error() == ""
     assert lib.gdn_conv_step(ctypes.byref(dims), None, None, None, None, None, None) == gdn.GDN_OK
     assert lib.gdn_rollback(ctypes.byref(dims), None, None, None, None, None, None, None, None) == gdn.GDN_OK
@@ -79,13 +81,13 @@ def test_empty_batch_is_a_noop(lib):
 
 def test_null_and_misaligned_pointers(lib):
     dims = gdn.make_dims(**BASE)
-    for i in range(13):
+    for i in range(NV):
         if i in (8,):          # conv_inter is optional
             continue
-        ptrs = _ptrs(13)
+        ptrs = _ptrs(NV)
         ptrs[i] = None
         assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_INVALID_ARG, i
-        ptrs = _ptrs(13)
+        ptrs = _ptrs(NV)
         ptrs[i] = ctypes.c_void_p(P + i * MB + 4)
         assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_INVALID_ARG, i
         assert "aligned" in gdn.last_error()
@@ -94,25 +96,39 @@ def test_null_and_misaligned_pointers(lib):
 def test_aliasing_rules(lib):
     dims = gdn.make_dims(**BASE)
     # out overlapping x
-    ptrs = _ptrs(13)
+    ptrs = _ptrs(NV)
     ptrs[12] = ptrs[0]
     assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_ALIAS
     # state_out partially overlapping state_in (shifted by 16 bytes)
-    ptrs = _ptrs(13)
+    ptrs = _ptrs(NV)
     ptrs[10] = ctypes.c_void_p(ptrs[9].value + 16)
     assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_ALIAS
     # state_inter overlapping state_out
-    ptrs = _ptrs(13)
+    ptrs = _ptrs(NV)
     ptrs[11] = ctypes.c_void_p(ptrs[10].value + 64)
     assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_ALIAS
     # conv_inter overlapping conv_state_in
-    ptrs = _ptrs(13)
+    ptrs = _ptrs(NV)
     ptrs[8] = ptrs[6]
     assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_ALIAS
     # K > 1 needs state_inter
-    ptrs = _ptrs(13)
+    ptrs = _ptrs(NV)
     ptrs[11] = None
     assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_INVALID_ARG
+    # workspace overlapping out, and a workspace that is too small
+    ptrs = _ptrs(NV)
+    ptrs[13] = ptrs[12]
+    assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_ALIAS
+    ptrs = _ptrs(NV)
+    assert _verify(lib, dims, ptrs, ws_bytes=64) == gdn.GDN_ERR_INVALID_ARG
+    assert "workspace" in gdn.last_error()
+
+
+def test_workspace_size_formula(lib):
+    dims = gdn.make_dims(B=32, K=16, Hk=16, Hv=32, dk=128, dv=128)
+    assert gdn.gdn_verify_workspace_size(dims) == 4 * (32 * 16 * (32 * 128 + 16 * 128) + 32 * 32 * 596)
+    with pytest.raises(gdn.GdnError):
+        gdn.gdn_verify_workspace_size(gdn.make_dims(B=1, K=0, Hk=1, Hv=1, dk=64, dv=64))
 
 
 def test_rollback_validation(lib):

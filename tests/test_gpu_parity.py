@@ -1,7 +1,7 @@
 """Parity of the sm_103a path (through the C ABI) with the CPU oracle.
 
 Inputs come from the seeded generator; expected values only from oracle/.  Sizes span
-several row tiles and clusters with ragged windows (odd K, odd B), every supported head
+several row tiles and head groups with ragged windows (odd K, odd B), every supported head
 shape, both output types, in place and ping-pong states, and the named workloads at their
 full sizes (all outputs, or sampled sequences / layers where the oracle would be slow).
 """
@@ -48,7 +48,7 @@ def _check_round(st, ref, d, out_f32=True, verified_state=None):
 
 
 SHAPES = [
-    # B, K, Hk, Hv, dk, dv   (row tile 32 or 64, clusters of 2..8 CTAs)
+    # B, K, Hk, Hv, dk, dv   (head groups r = 1..5, dk and dv 64 or 128)
     (3, 5, 2, 4, 128, 128),
     (2, 16, 1, 3, 128, 128),
     (2, 7, 2, 2, 64, 128),
@@ -78,8 +78,8 @@ def test_shapes_against_oracle(shape, out_f32):
     np.testing.assert_array_equal(st.conv_state.cpu().numpy(), ref["conv_state_out"])
 
 
-def test_eight_vheads_per_qk_head_cluster_of_16():
-    """Hv/Hk = 8 with dv = 128 runs as clusters of 16 CTAs (non-portable size)."""
+def test_many_vheads_per_qk_head():
+    """Hv/Hk = 8: one q/k head feeds eight v-heads (the prologue writes eight gate blocks)."""
     d = Dims(B=2, K=6, Hk=1, Hv=8, dk=128, dv=128)
     g = Gen(77)
     lay = make_layer(g, d, Dists())
@@ -222,7 +222,7 @@ def test_empty_batch_through_binding():
     e = torch.empty(0, device="cuda")
     eb = torch.empty(0, device="cuda", dtype=torch.bfloat16)
     gdn.gdn_verify_step(dims, eb, eb, eb, torch.zeros(4, device="cuda"), torch.zeros(4, device="cuda"),
-                        torch.zeros(d.C * 4, device="cuda"), e, e, e, e, e, e, e)
+                        torch.zeros(d.C * 4, device="cuda"), e, e, e, e, e, e, e, None)
 
 
 def test_decode_workload_1000_carried_steps():
