@@ -129,6 +129,31 @@ gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16
 gdn_status gdn_verify_workspace_size(const gdn_dims* dims, uint64_t* bytes);
 
 /*
+ * gdn_verify_step for callers that cannot allocate device memory.  (The pages
+ * have no counterpart: this is a convenience of this library.)
+ *
+ * Same arguments and results as gdn_verify_step minus the workspace.  Some
+ * callers may not call cudaMalloc where they run the verify step (a runtime
+ * whose memory pool forbids allocation on its hot path, a path that must not
+ * synchronise the device, an embedder that only passes in tensors it owns);
+ * this entry point takes its scratch from a fixed 16 MiB array in the
+ * library's device memory instead, enough for B = 32 at Hk = 16, Hv = 32,
+ * dk = 128.  Every GPU that loads the library holds that array until the
+ * process exits.  Larger dims return GDN_ERR_UNSUPPORTED with a message.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current and caches it: make the
+ *    first call on a device before any stream capture starts.
+ *  - The scratch needs no zeroing; nothing is allocated or freed.
+ *  - All calls on a device share the array: calls whose kernels may overlap
+ *    on the GPU (unordered streams) race on it and must be serialised.
+ */
+gdn_status gdn_verify_step_static_scratch(const gdn_dims* dims, const uint16_t* x, const uint16_t* a,
+                                          const uint16_t* b, const float* A_log, const float* dt_bias,
+                                          const float* conv_w, const float* conv_state_in, float* conv_state_out,
+                                          float* conv_inter, const float* state_in, float* state_out,
+                                          float* state_inter, void* out, gdn_stream_t stream);
+
+/*
  * a5: per sequence, keep the first L = accept_len[b] window tokens
  * (strix-llama.cpp #14: snapshot restore of the recurrent state; lucebox #637:
  * rollback window copy of the conv history).

@@ -101,6 +101,10 @@ gdn_status check_dims(const gdn_dims* d, bool need_gates) {
 
 }  // namespace
 
+namespace gdn {
+gdn_status report_error(gdn_status s, const char* msg) { return fail(s, "%s", msg); }
+}  // namespace gdn
+
 extern "C" {
 
 const char* gdn_last_error(void) { return g_last_error.c_str(); }

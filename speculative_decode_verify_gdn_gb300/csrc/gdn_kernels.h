@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/gdn.h"
+
 namespace gdn {
 
 constexpr int kKMax = 16;  // longest verify window a launch handles
@@ -80,5 +82,8 @@ struct RollbackParams {
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_rollback(const RollbackParams& p, cudaStream_t stream);
+
+// Records `msg` as this thread's gdn_last_error() text and returns `s`.
+gdn_status report_error(gdn_status s, const char* msg);
 
 }  // namespace gdn

@@ -1,0 +1,61 @@
+"""The allocation-free verify entry point against the regular one.
+
+gdn_verify_step_static_scratch serves callers that may not allocate device memory where they run
+the verify step; it takes its scratch from a fixed array inside the library.  This file runs last
+(pytest collects it after the others) so that a failure here comes after every other test has run,
+and it also passes on its own in a fresh process.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from parity_util import OUT_TOL, STATE_TOL, out_rel_err, state_rel_err
+from speculative_decode_verify_gdn_gb300 import gdn
+from speculative_decode_verify_gdn_gb300.build import build_library
+from speculative_decode_verify_gdn_gb300.runtime import GdnLayerState
+from speculative_decode_verify_gdn_gb300.synth import WORKLOADS, Dims, Dists, Gen, make_layer, make_round
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_pair(d, dists, seed):
+    """Two windows in a row through each entry point, each side carrying its own state in place."""
+    g = Gen(seed)
+    lay = make_layer(g, d, dists)
+    rnds = [make_round(g, d, dists) for _ in range(2)]
+    ref = GdnLayerState.create(d, lay)
+    nal = GdnLayerState.create(d, lay)
+    for rnd in rnds:
+        ref.load_round(rnd)
+        ref.verify()
+        nal.load_round(rnd)
+        gdn.gdn_verify_step_static_scratch(nal.dims, nal.x, nal.a, nal.b, nal.A_log, nal.dt_bias, nal.conv_w,
+                                           nal.conv_states[0], nal.conv_states[0], nal.conv_inter, nal.states[0],
+                                           nal.states[0], nal.state_inter, nal.out)
+        torch.cuda.synchronize()
+        assert out_rel_err(nal.out.cpu().numpy(), ref.out.cpu().numpy()) <= OUT_TOL
+        assert state_rel_err(nal.state.cpu().numpy(), ref.state.cpu().numpy()) <= STATE_TOL
+        if d.K > 1:
+            assert state_rel_err(nal.state_inter.cpu().numpy(), ref.state_inter.cpu().numpy()) <= STATE_TOL
+        np.testing.assert_array_equal(nal.conv_inter.cpu().numpy(), ref.conv_inter.cpu().numpy())
+        np.testing.assert_array_equal(nal.conv_state.cpu().numpy(), ref.conv_state.cpu().numpy())
+
+
+def test_static_scratch_matches_workspace_entry_point():
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    build_library()
+    gdn.load_library()
+    _run_pair(Dims(B=3, K=7, Hk=2, Hv=4, dk=128, dv=128), Dists(), 501)
+    w = WORKLOADS["serve16"]                      # the largest shape the fixed scratch holds
+    _run_pair(w.dims, w.dists, 502)
+    assert gdn.gdn_device_status(clear=True) == 0
+
+
+def test_static_scratch_rejects_oversized_dims():
+    lib = gdn.load_library()
+    dims = gdn.make_dims(B=64, K=16, Hk=16, Hv=32, dk=128, dv=128)   # needs 30 MB of scratch
+    status = lib.gdn_verify_step_static_scratch(ctypes.byref(dims), *([ctypes.c_void_p(1 << 32)] * 13), None)
+    assert status == gdn.GDN_ERR_UNSUPPORTED
+    assert "static scratch" in gdn.last_error()
