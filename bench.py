@@ -270,6 +270,29 @@ def run_gdn(args):
     ms = max_over_ranks(ms, world, dev)
     value = job_throughput(d.B * d.K * args.steps, world, ms)
 
+    # the same steps with each window's rollback applied on the next verify's read
+    # (gdn_verify_resume): no rollback copy, one verify call per step
+    def resume_step(i):
+        j, jp = i % n_in, (i - 1) % n_in
+        gdn.gdn_verify_resume(dims, accs[jp], xs[j], as_[j], bs[j], st.A_log, st.dt_bias, st.conv_w, CS, CI, None,
+                              CS, CI, S0, SI, None, S0, SI, OUT, WS, stream)
+
+    for i in range(args.warmup):
+        resume_step(i + 1)
+    barrier()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    for i in range(args.steps):
+        resume_step(args.warmup + 1 + i)
+    r1.record(stream)
+    barrier()
+    rms = max_over_ranks(r0.elapsed_time(r1), world, dev)
+    resume = {"value": job_throughput(d.B * d.K * args.steps, world, rms), "unit": UNIT,
+              "ms_per_step": rms / args.steps, "gpu_launches": 2 * args.steps,
+              "what": "gdn_verify_resume per step: the previous window's rollback applied on read, no copy"}
+    if gdn.gdn_device_status(clear=True):
+        raise RuntimeError("device status flags after the resume steps")
+
     # e2e: inputs from pinned host memory and the output back, inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -330,6 +353,7 @@ def run_gdn(args):
         "e2e": e2e,
         "clocks": clocks.summary(),
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "zero_copy_rollback": resume,
     }
     if world > 1:
         dist.barrier()

@@ -123,6 +123,36 @@ gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16
                            void* workspace, uint64_t workspace_bytes, gdn_stream_t stream);
 
 /*
+ * a5 of the previous window fused into a1..a4 of the next one: rollback applied
+ * on read, so the accepted state is never copied (strix-llama.cpp #14: snapshot
+ * planes and rolling checkpoints; atlas #297: per-token intermediates kept for
+ * partial-accept rollback).  Same result as
+ *   gdn_rollback(accept_len_prev, ...) followed by gdn_verify_step(...),
+ * where the previous window had the same K.  Per sequence, with
+ * L = accept_len_prev[b]:
+ *   L == K       S0 = state_in[b],                  history = conv_state_in[b]
+ *   1 <= L < K   S0 = state_inter_prev[b][L-1],     history = conv_inter_prev[b][L-1]
+ *   L == 0       S0 = state_snapshot_prev[b],       history = conv_state_snapshot_prev[b]
+ * state_in / conv_state_in are the previous window's final state and history;
+ * the *_prev buffers its intermediates and the pre-window snapshots (both
+ * snapshots or neither; NULL makes L == 0 an error).  An out-of-range L, or
+ * L == 0 without snapshots, is read as L == K and sets a device status bit.
+ * In place is allowed and is the intended use: state_out may be state_in or
+ * state_snapshot_prev, state_inter may be state_inter_prev, conv_state_out may
+ * be conv_state_in or conv_state_snapshot_prev, conv_inter may be
+ * conv_inter_prev (each state tile and history channel is read, then
+ * rewritten, by one owner).  Any other overlap with an output is rejected.
+ * Shapes, workspace and the remaining arguments as gdn_verify_step.
+ */
+gdn_status gdn_verify_resume(const gdn_dims* dims, const int32_t* accept_len_prev, const uint16_t* x,
+                             const uint16_t* a, const uint16_t* b, const float* A_log, const float* dt_bias,
+                             const float* conv_w, const float* conv_state_in, const float* conv_inter_prev,
+                             const float* conv_state_snapshot_prev, float* conv_state_out, float* conv_inter,
+                             const float* state_in, const float* state_inter_prev, const float* state_snapshot_prev,
+                             float* state_out, float* state_inter, void* out, void* workspace,
+                             uint64_t workspace_bytes, gdn_stream_t stream);
+
+/*
  * Bytes of workspace gdn_verify_step needs for `dims`:
  * 4 * (B*Hk*(32*dk + 16*dk) + B*Hv*596).  Validates dims like gdn_verify_step.
  */

@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <mutex>
 #include <string>
 
@@ -99,6 +100,154 @@ gdn_status check_dims(const gdn_dims* d, bool need_gates) {
     if ((p) && !aligned16(p)) return fail(GDN_ERR_INVALID_ARG, "%s is not 16-byte aligned", name); \
   } while (0)
 
+// Arguments of the verify step; the *_prev and snapshot fields are used by gdn_verify_resume only.
+struct VerifyArgs {
+  bool resume;
+  const int32_t* accept_prev;
+  const uint16_t *x, *a, *b;
+  const float *A_log, *dt_bias, *conv_w;
+  const float* conv_state_in;
+  const float* conv_inter_prev;
+  const float* conv_snap_prev;
+  float* conv_state_out;
+  float* conv_inter;
+  const float* state_in;
+  const float* state_inter_prev;
+  const float* state_snap_prev;
+  float* state_out;
+  float* state_inter;
+  void* out;
+  void* workspace;
+  uint64_t workspace_bytes;
+};
+
+struct Buf {
+  const char* name;
+  Range r;
+  bool output;
+};
+
+gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t stream) {
+  gdn_status s = check_dims(dims, true);
+  if (s != GDN_OK) return s;
+  const gdn_dims& d = *dims;
+  if (d.B == 0) return ok();
+  GDN_CHECK_PTR(v.x, "x");
+  GDN_CHECK_PTR(v.a, "a");
+  GDN_CHECK_PTR(v.b, "b");
+  GDN_CHECK_PTR(v.A_log, "A_log");
+  GDN_CHECK_PTR(v.dt_bias, "dt_bias");
+  GDN_CHECK_PTR(v.conv_w, "conv_w");
+  GDN_CHECK_PTR(v.conv_state_in, "conv_state_in");
+  GDN_CHECK_PTR(v.conv_state_out, "conv_state_out");
+  GDN_CHECK_OPT_PTR(v.conv_inter, "conv_inter");
+  GDN_CHECK_PTR(v.state_in, "state_in");
+  GDN_CHECK_PTR(v.state_out, "state_out");
+  GDN_CHECK_OPT_PTR(v.state_inter, "state_inter");
+  GDN_CHECK_PTR(v.out, "out");
+  GDN_CHECK_PTR(v.workspace, "workspace");
+  if (d.K > 1 && !v.state_inter) return fail(GDN_ERR_INVALID_ARG, "state_inter is NULL with K=%d > 1", d.K);
+  if (v.resume) {
+    if (!v.accept_prev) return fail(GDN_ERR_INVALID_ARG, "accept_len_prev is NULL");
+    if (reinterpret_cast<uintptr_t>(v.accept_prev) & 3u) return fail(GDN_ERR_INVALID_ARG, "accept_len_prev misaligned");
+    GDN_CHECK_OPT_PTR(v.state_inter_prev, "state_inter_prev");
+    GDN_CHECK_OPT_PTR(v.conv_inter_prev, "conv_inter_prev");
+    GDN_CHECK_OPT_PTR(v.state_snap_prev, "state_snapshot_prev");
+    GDN_CHECK_OPT_PTR(v.conv_snap_prev, "conv_state_snapshot_prev");
+    if (d.K > 1 && (!v.state_inter_prev || !v.conv_inter_prev))
+      return fail(GDN_ERR_INVALID_ARG, "state_inter_prev and conv_inter_prev are required when K=%d > 1", d.K);
+    if ((v.state_snap_prev == nullptr) != (v.conv_snap_prev == nullptr))
+      return fail(GDN_ERR_NO_SNAPSHOT, "pass both snapshots or neither");
+  }
+  const size_t ws_need = gdn::workspace_bytes(d.B, d.Hk, d.Hv, d.dk);
+  if (v.workspace_bytes < ws_need)
+    return fail(GDN_ERR_INVALID_ARG, "workspace has %llu bytes, needs %zu", (unsigned long long)v.workspace_bytes,
+                ws_need);
+
+  const size_t C = 2ull * d.Hk * d.dk + size_t(d.Hv) * d.dv;
+  const size_t B = size_t(d.B), K = size_t(d.K);
+  const size_t S = size_t(d.Hv) * d.dv * d.dk;  // state floats per sequence
+  const bool k1 = d.K == 1;
+  const Buf bufs[] = {
+      {"x", range_of(v.x, B * K * C * 2), false},
+      {"a", range_of(v.a, B * K * d.Hv * 2), false},
+      {"b", range_of(v.b, B * K * d.Hv * 2), false},
+      {"A_log", range_of(v.A_log, size_t(d.Hv) * 4), false},
+      {"dt_bias", range_of(v.dt_bias, size_t(d.Hv) * 4), false},
+      {"conv_w", range_of(v.conv_w, C * 4 * 4), false},
+      {"conv_state_in", range_of(v.conv_state_in, B * 3 * C * 4), false},
+      {"conv_inter_prev", range_of(k1 ? nullptr : v.conv_inter_prev, B * K * 3 * C * 4), false},
+      {"conv_state_snapshot_prev", range_of(v.conv_snap_prev, B * 3 * C * 4), false},
+      {"state_in", range_of(v.state_in, B * S * 4), false},
+      {"state_inter_prev", range_of(k1 ? nullptr : v.state_inter_prev, B * (K - 1) * S * 4), false},
+      {"state_snapshot_prev", range_of(v.state_snap_prev, B * S * 4), false},
+      {"accept_len_prev", range_of(v.accept_prev, B * 4), false},
+      {"conv_state_out", range_of(v.conv_state_out, B * 3 * C * 4), true},
+      {"conv_inter", range_of(v.conv_inter, B * K * 3 * C * 4), true},
+      {"state_out", range_of(v.state_out, B * S * 4), true},
+      {"state_inter", range_of(k1 ? nullptr : v.state_inter, B * (K - 1) * S * 4), true},
+      {"out", range_of(v.out, B * K * d.Hv * d.dv * (d.out_f32 ? 4 : 2)), true},
+      {"workspace", range_of(v.workspace, ws_need), true},
+  };
+  // (output, input) pairs that may be the very same buffer: every state tile and every history
+  // channel is read, then rewritten, by one owner, so working in place is race-free
+  const char* in_place[][2] = {{"conv_state_out", "conv_state_in"},       {"state_out", "state_in"},
+                               {"conv_inter", "conv_inter_prev"},         {"state_inter", "state_inter_prev"},
+                               {"conv_state_out", "conv_state_snapshot_prev"}, {"state_out", "state_snapshot_prev"}};
+  const int n = int(sizeof(bufs) / sizeof(bufs[0]));
+  for (int i = 0; i < n; ++i) {
+    if (!bufs[i].output) continue;
+    for (int j = 0; j < n; ++j) {
+      if (i == j || (bufs[j].output && j < i) || !overlap(bufs[i].r, bufs[j].r)) continue;
+      bool allowed = false;
+      if (!bufs[j].output && bufs[i].r.lo == bufs[j].r.lo && bufs[i].r.hi == bufs[j].r.hi)
+        for (const auto& pr : in_place)
+          if (!strcmp(pr[0], bufs[i].name) && !strcmp(pr[1], bufs[j].name)) allowed = true;
+      if (!allowed) return fail(GDN_ERR_ALIAS, "%s overlaps %s", bufs[i].name, bufs[j].name);
+    }
+  }
+
+  uint32_t* err = nullptr;
+  s = status_word(&err);
+  if (s != GDN_OK) return s;
+  gdn::VerifyParams p{};
+  p.x = v.x;
+  p.a = v.a;
+  p.b = v.b;
+  p.A_log = v.A_log;
+  p.dt_bias = v.dt_bias;
+  p.conv_w = v.conv_w;
+  p.conv_state_in = v.conv_state_in;
+  p.conv_state_out = v.conv_state_out;
+  p.conv_inter = v.conv_inter;
+  p.state_in = v.state_in;
+  p.state_out = v.state_out;
+  p.state_inter = k1 ? nullptr : v.state_inter;
+  p.out = v.out;
+  p.ws = gdn::workspace_carve(v.workspace, d.B, d.Hk, d.Hv, d.dk);
+  if (v.resume) {
+    p.accept_prev = v.accept_prev;
+    p.state_inter_prev = k1 ? nullptr : v.state_inter_prev;
+    p.conv_inter_prev = k1 ? nullptr : v.conv_inter_prev;
+    p.state_snap_prev = v.state_snap_prev;
+    p.conv_snap_prev = v.conv_snap_prev;
+  }
+  p.err = err;
+  p.B = d.B;
+  p.K = d.K;
+  p.Hk = d.Hk;
+  p.Hv = d.Hv;
+  p.dk = d.dk;
+  p.dv = d.dv;
+  p.C = int(C);
+  p.q_scale = d.q_scale;
+  p.l2_eps = d.l2_eps;
+  p.out_f32 = d.out_f32;
+  cudaError_t e = gdn::launch_verify(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "verify launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 }  // namespace
 
 namespace gdn {
@@ -165,90 +314,55 @@ gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16
                            const float* conv_state_in, float* conv_state_out, float* conv_inter,
                            const float* state_in, float* state_out, float* state_inter, void* out,
                            void* workspace, uint64_t workspace_bytes, gdn_stream_t stream) {
-  gdn_status s = check_dims(dims, true);
-  if (s != GDN_OK) return s;
-  const gdn_dims& d = *dims;
-  if (d.B == 0) return ok();
-  GDN_CHECK_PTR(x, "x");
-  GDN_CHECK_PTR(a, "a");
-  GDN_CHECK_PTR(b, "b");
-  GDN_CHECK_PTR(A_log, "A_log");
-  GDN_CHECK_PTR(dt_bias, "dt_bias");
-  GDN_CHECK_PTR(conv_w, "conv_w");
-  GDN_CHECK_PTR(conv_state_in, "conv_state_in");
-  GDN_CHECK_PTR(conv_state_out, "conv_state_out");
-  GDN_CHECK_OPT_PTR(conv_inter, "conv_inter");
-  GDN_CHECK_PTR(state_in, "state_in");
-  GDN_CHECK_PTR(state_out, "state_out");
-  GDN_CHECK_OPT_PTR(state_inter, "state_inter");
-  GDN_CHECK_PTR(out, "out");
-  GDN_CHECK_PTR(workspace, "workspace");
-  if (d.K > 1 && !state_inter) return fail(GDN_ERR_INVALID_ARG, "state_inter is NULL with K=%d > 1", d.K);
-  const size_t ws_need = gdn::workspace_bytes(d.B, d.Hk, d.Hv, d.dk);
-  if (workspace_bytes < ws_need)
-    return fail(GDN_ERR_INVALID_ARG, "workspace has %llu bytes, needs %zu", (unsigned long long)workspace_bytes, ws_need);
+  VerifyArgs v{};
+  v.x = x;
+  v.a = a;
+  v.b = b;
+  v.A_log = A_log;
+  v.dt_bias = dt_bias;
+  v.conv_w = conv_w;
+  v.conv_state_in = conv_state_in;
+  v.conv_state_out = conv_state_out;
+  v.conv_inter = conv_inter;
+  v.state_in = state_in;
+  v.state_out = state_out;
+  v.state_inter = state_inter;
+  v.out = out;
+  v.workspace = workspace;
+  v.workspace_bytes = workspace_bytes;
+  return verify_impl(dims, v, stream);
+}
 
-  const size_t C = 2ull * d.Hk * d.dk + size_t(d.Hv) * d.dv;
-  const size_t B = size_t(d.B), K = size_t(d.K);
-  const size_t S = size_t(d.Hv) * d.dv * d.dk;  // state floats per sequence
-  const Range r_x = range_of(x, B * K * C * 2), r_a = range_of(a, B * K * d.Hv * 2),
-              r_b = range_of(b, B * K * d.Hv * 2), r_alog = range_of(A_log, size_t(d.Hv) * 4),
-              r_dt = range_of(dt_bias, size_t(d.Hv) * 4), r_w = range_of(conv_w, C * 4 * 4),
-              r_csi = range_of(conv_state_in, B * 3 * C * 4), r_cso = range_of(conv_state_out, B * 3 * C * 4),
-              r_ci = range_of(conv_inter, B * K * 3 * C * 4), r_si = range_of(state_in, B * S * 4),
-              r_so = range_of(state_out, B * S * 4),
-              r_sx = range_of(d.K > 1 ? state_inter : nullptr, B * (K - 1) * S * 4),
-              r_o = range_of(out, B * K * d.Hv * d.dv * (d.out_f32 ? 4 : 2)), r_ws = range_of(workspace, ws_need);
-  // in-place pairs: identical start or disjoint
-  if (conv_state_out != conv_state_in && overlap(r_cso, r_csi))
-    return fail(GDN_ERR_ALIAS, "conv_state_out partially overlaps conv_state_in");
-  if (state_out != state_in && overlap(r_so, r_si))
-    return fail(GDN_ERR_ALIAS, "state_out partially overlaps state_in");
-  const Range ins[7] = {r_x, r_a, r_b, r_alog, r_dt, r_w, r_csi};
-  const Range writes[6] = {r_cso, r_ci, r_so, r_sx, r_o, r_ws};
-  const char* wname[6] = {"conv_state_out", "conv_inter", "state_out", "state_inter", "out", "workspace"};
-  for (int i = 0; i < 6; ++i) {
-    for (int j = 0; j < 7; ++j) {
-      if (i == 0 && j == 6) continue;  // conv_state_out vs conv_state_in handled above
-      if (overlap(writes[i], ins[j])) return fail(GDN_ERR_ALIAS, "%s overlaps an input", wname[i]);
-    }
-    if (i != 2 && overlap(writes[i], r_si)) return fail(GDN_ERR_ALIAS, "%s overlaps state_in", wname[i]);
-    for (int j = i + 1; j < 6; ++j)
-      if (overlap(writes[i], writes[j])) return fail(GDN_ERR_ALIAS, "%s overlaps %s", wname[i], wname[j]);
-  }
-
-  uint32_t* err = nullptr;
-  s = status_word(&err);
-  if (s != GDN_OK) return s;
-  gdn::VerifyParams p{};
-  p.x = x;
-  p.a = a;
-  p.b = b;
-  p.A_log = A_log;
-  p.dt_bias = dt_bias;
-  p.conv_w = conv_w;
-  p.conv_state_in = conv_state_in;
-  p.conv_state_out = conv_state_out;
-  p.conv_inter = conv_inter;
-  p.state_in = state_in;
-  p.state_out = state_out;
-  p.state_inter = d.K > 1 ? state_inter : nullptr;
-  p.out = out;
-  p.ws = gdn::workspace_carve(workspace, d.B, d.Hk, d.Hv, d.dk);
-  p.err = err;
-  p.B = d.B;
-  p.K = d.K;
-  p.Hk = d.Hk;
-  p.Hv = d.Hv;
-  p.dk = d.dk;
-  p.dv = d.dv;
-  p.C = int(C);
-  p.q_scale = d.q_scale;
-  p.l2_eps = d.l2_eps;
-  p.out_f32 = d.out_f32;
-  cudaError_t e = gdn::launch_verify(p, reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "verify_step launch: %s", cudaGetErrorString(e));
-  return ok();
+gdn_status gdn_verify_resume(const gdn_dims* dims, const int32_t* accept_len_prev, const uint16_t* x,
+                             const uint16_t* a, const uint16_t* b, const float* A_log, const float* dt_bias,
+                             const float* conv_w, const float* conv_state_in, const float* conv_inter_prev,
+                             const float* conv_state_snapshot_prev, float* conv_state_out, float* conv_inter,
+                             const float* state_in, const float* state_inter_prev, const float* state_snapshot_prev,
+                             float* state_out, float* state_inter, void* out, void* workspace,
+                             uint64_t workspace_bytes, gdn_stream_t stream) {
+  VerifyArgs v{};
+  v.resume = true;
+  v.accept_prev = accept_len_prev;
+  v.x = x;
+  v.a = a;
+  v.b = b;
+  v.A_log = A_log;
+  v.dt_bias = dt_bias;
+  v.conv_w = conv_w;
+  v.conv_state_in = conv_state_in;
+  v.conv_inter_prev = conv_inter_prev;
+  v.conv_snap_prev = conv_state_snapshot_prev;
+  v.conv_state_out = conv_state_out;
+  v.conv_inter = conv_inter;
+  v.state_in = state_in;
+  v.state_inter_prev = state_inter_prev;
+  v.state_snap_prev = state_snapshot_prev;
+  v.state_out = state_out;
+  v.state_inter = state_inter;
+  v.out = out;
+  v.workspace = workspace;
+  v.workspace_bytes = workspace_bytes;
+  return verify_impl(dims, v, stream);
 }
 
 gdn_status gdn_rollback(const gdn_dims* dims, const int32_t* accept_len_dev, const float* state_in_snapshot,

@@ -88,7 +88,9 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
 }
 
 // ---------------------------------------------------------------- misc math helpers
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+// SiLU(z) = z / (1 + e^-z) with the fast exp and divide intrinsics (a few ulp; for z below about
+// -88 the denominator overflows and the result is 0, where SiLU is below 1e-36 in magnitude).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

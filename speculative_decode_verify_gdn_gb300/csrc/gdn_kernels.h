@@ -13,7 +13,8 @@ constexpr int kKMax = 16;  // longest verify window a launch handles
 constexpr int kConvW = 4;  // conv taps
 constexpr int kNCol = 2 * kKMax;  // columns of the normalised q/k table: k^ in [0,16), q^ in [16,32)
 constexpr int kMStride = kKMax + 1;
-// Per-(sequence, v-head) gate block: M[16][17], N[16][17], beta[16], g[16], Gamma[16], padding.
+// Per-(sequence, v-head) gate block: M[16][17] = D (k^.k^) strictly lower, N[16][17] =
+// q_scale D (k^.q^) lower, beta[16], g[16], Gamma[16], padding (D: decay products).
 constexpr int kGateFloats = 2 * kKMax * kMStride + 3 * kKMax + 4;  // 596 floats = 2384 bytes (16-byte multiple)
 constexpr int kGateOffN = kKMax * kMStride;
 constexpr int kGateOffBeta = 2 * kKMax * kMStride;
@@ -21,10 +22,9 @@ constexpr int kGateOffG = kGateOffBeta + kKMax;
 constexpr int kGateOffGam = kGateOffG + kKMax;
 
 // Workspace written by the q/k prologue kernel and read by the state kernel:
-//   wt   [B][Hk][dk][32]   normalised k^ (columns 0..15) and q^ (16..31), column index
-//                          swizzled as col ^ (c & 31) so both kernels access it conflict-free
-//   kn   [B][Hk][16][dk]   normalised k^, token-major
-//   gate [B][Hv][kGateFloats]
+//   wt    [B][Hk][dk][32]     normalised k^ (columns 0..15) and q^ (16..31)
+//   kn    [B][Hk][16][dk]     normalised k^, token-major
+//   gate  [B][Hv][kGateFloats]
 struct Workspace {
   float* wt;
   float* kn;
@@ -49,6 +49,16 @@ struct VerifyParams {
   float* state_inter;  // null only when K == 1
   void* out;
   Workspace ws;
+  // Rollback of the previous window applied on read (all null for a plain verify step): per
+  // sequence, L = accept_prev[b] selects where S0 and the conv history come from -
+  // L == K: state_in / conv_state_in (the previous window's final state and history);
+  // 1 <= L < K: state_inter_prev[b][L-1] / conv_inter_prev[b][L-1];
+  // L == 0: state_snap_prev / conv_snap_prev (the state before the previous window).
+  const int32_t* accept_prev;
+  const float* state_inter_prev;
+  const float* conv_inter_prev;
+  const float* state_snap_prev;  // may be null (then L == 0 is an error)
+  const float* conv_snap_prev;
   uint32_t* err;       // device status word
   int B, K, Hk, Hv, dk, dv, C;
   float q_scale, l2_eps;

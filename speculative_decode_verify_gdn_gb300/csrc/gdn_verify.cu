@@ -25,13 +25,13 @@
 //  1. qk_prologue: one CTA per (sequence, q/k head).  Conv + SiLU of the head's q|k channels
 //     (each channel's history is read and rewritten by this one thread, so the in-place
 //     history update is race-free), L2 norms, gates of the head's r = Hv/Hk v-heads, Gram
-//     products and decay products.  Writes three small tables per head to the workspace, laid
-//     out exactly as the second kernel keeps them in shared memory.
+//     products and decay products.  Writes small per-head tables to the workspace, laid out as
+//     the second kernel keeps them in shared memory.
 //  2. state_stream: one CTA per (sequence, v-head, 32-row tile of the state), launched with
 //     programmatic dependent launch so that it starts while the prologue runs: it issues the
 //     bulk async (TMA) copy of its 16 KB S0 tile and convolves its own 32 v-channels first, then
 //     waits for the prologue grid and bulk-copies the tables.  From there each warp owns four
-//     state rows and needs no CTA-wide barrier: products with S0, forward substitution,
+//     state rows and needs no further CTA-wide barrier: products with S0, forward substitution,
 //     outputs, then the K states leave straight from registers as coalesced 16-byte streaming
 //     stores (512 contiguous bytes per warp instruction).
 #include "gdn_common.cuh"
@@ -68,13 +68,38 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 // Index of q^/k^ column `col` of channel `c` in the swizzled table.
 __device__ __forceinline__ int wt_idx(int c, int col) { return c * kNCol + (col ^ (c & 31)); }
 
-// Conv + SiLU of one channel over the window; writes the channel's history snapshots and new
-// history.  y[t] receives the outputs for t < K.
+// Accepted length of the previous window for sequence b, or -1 for a plain verify step (no
+// rollback applied on read).  Lengths outside 0..K, and 0 without a snapshot, read as K (the
+// previous final state) after flagging the device status word.
+__device__ __forceinline__ int prev_accept(const VerifyParams& p, int b, bool report) {
+  if (!p.accept_prev) return -1;
+  const int L = p.accept_prev[b];
+  if (L < 0 || L > p.K) {
+    if (report) atomicOr(p.err, kDevErrAcceptRange);
+    return p.K;
+  }
+  if (L == 0 && !p.state_snap_prev) {
+    if (report) atomicOr(p.err, kDevErrNoSnapshot);
+    return p.K;
+  }
+  return L;
+}
+
+// Where channel c's history before this window starts, [3] rows C apart.
+__device__ __forceinline__ const float* history_src(const VerifyParams& p, int b, int c, int L) {
+  const int C = p.C;
+  if (L < 0 || L == p.K) return p.conv_state_in + size_t(b) * 3 * C + c;
+  if (L == 0) return p.conv_snap_prev + size_t(b) * 3 * C + c;
+  return p.conv_inter_prev + (size_t(b) * p.K + (L - 1)) * 3 * C + c;
+}
+
+// Conv + SiLU of one channel over the window; writes the channel's K history snapshots (if
+// requested) and its new history.  y[t] receives the outputs for t < K.
 __device__ __forceinline__ void conv_channel(const VerifyParams& p, int b, int c, float (&y)[kKMax]) {
   const int C = p.C;
   const int K = p.K;
   const float4 w = *reinterpret_cast<const float4*>(p.conv_w + size_t(c) * kConvW);
-  const float* hin = p.conv_state_in + size_t(b) * 3 * C + c;
+  const float* hin = history_src(p, b, c, prev_accept(p, b, false));
   float h0 = hin[0], h1 = hin[C], h2 = hin[2 * C];
   const uint16_t* xp = p.x + size_t(b) * K * C + c;
   float xv[kKMax];
@@ -107,28 +132,42 @@ __device__ __forceinline__ void conv_channel(const VerifyParams& p, int b, int c
 // Kernel 1: per (sequence, q/k head) prologue.
 template <int DK>
 struct PrologueLayout {
-  static constexpr int NSTRIDE = DK + 1;                    // padded rows: column reads conflict-free
   static constexpr int OFF_Y = 0;                           // raw conv outputs [32][DK] (k: 0..15, q: 16..31)
-  static constexpr int OFF_N = OFF_Y + kNCol * DK;          // normalised [32][NSTRIDE]
-  static constexpr int OFF_KK = OFF_N + kNCol * NSTRIDE;    // k^_t . k^_j  [16][17]
+  static constexpr int OFF_T = OFF_Y + kNCol * DK;          // normalised table [DK][32], swizzled as in global
+  static constexpr int OFF_INV = OFF_T + DK * kNCol;        // 1 / sqrt(|y_n|^2 + eps) [32]
+  static constexpr int OFF_KK = OFF_INV + kNCol;            // k^_t . k^_j  [16][17]
   static constexpr int OFF_KQ = OFF_KK + kKMax * kMStride;  // k^_j . q^_t  [16][17]
-  static constexpr int OFF_BG = OFF_KQ + kKMax * kMStride;  // beta[16], g[16] of one v-head
-  static constexpr int FLOATS = OFF_BG + 2 * kKMax;
+  static constexpr int OFF_BG = OFF_KQ + kKMax * kMStride;  // beta, g of up to 16 v-heads [16][2][16]
+  static constexpr int FLOATS = OFF_BG + 16 * 2 * kKMax;
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
+  static_assert(OFF_T % 4 == 0 && OFF_BG % 4 == 0, "float4 access");
 };
 
+// Butterfly reduce-scatter of 32 values per lane across the warp: on return v[0] holds the warp
+// sum of value `lane` (five halvings, 31 shuffles per lane).
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[32], int lane) {
+#pragma unroll
+  for (int d = 16, half = 16; d >= 1; d >>= 1, half >>= 1) {
+    const bool upper = (lane & d) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+    }
+  }
+}
+
 template <int DK>
-__global__ void __launch_bounds__(kThreads) gdn_qk_prologue_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const VerifyParams p) {
   using L = PrologueLayout<DK>;
   extern __shared__ __align__(128) float sm[];
   float* sY = sm + L::OFF_Y;
-  float* sN = sm + L::OFF_N;
+  float* sT = sm + L::OFF_T;
+  float* sInv = sm + L::OFF_INV;
   float* sKK = sm + L::OFF_KK;
   float* sKQ = sm + L::OFF_KQ;
-  float* sBeta = sm + L::OFF_BG;
-  float* sG = sBeta + kKMax;
-
-  griddep_launch_dependents();  // the state kernel may start its independent work now
+  float* sBG = sm + L::OFF_BG;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -137,8 +176,42 @@ __global__ void __launch_bounds__(kThreads) gdn_qk_prologue_kernel(const VerifyP
   const int b = blockIdx.y;
   const int K = p.K;
   const int r = p.Hv / p.Hk;
+  const size_t head = size_t(b) * p.Hk + kh;
 
-  // a1: conv of the head's q|k channels (thread cc < 2*DK owns one channel)
+  // a3 inputs of up to 16 v-heads (thread = (head, token)), loaded first so that their latency
+  // overlaps the conv's loads; the gates are evaluated once the conv is done
+  float ga = 0.f, gb = 0.f, gA = 0.f, gdt = 0.f;
+  auto gate_load = [&](int hv0) {
+    const int hv = hv0 + (tid >> 4), t = tid & 15;
+    if (hv < r && t < K) {
+      const int h = kh * r + hv;
+      const size_t gi = (size_t(b) * K + t) * p.Hv + h;
+      ga = bf16_to_f32(p.a[gi]);
+      gb = bf16_to_f32(p.b[gi]);
+      gA = p.A_log[h];
+      gdt = p.dt_bias[h];
+    }
+  };
+  auto gate_store = [&](int hv0) {
+    const int hv = hv0 + (tid >> 4), t = tid & 15;
+    if (hv < r) {
+      float beta = 0.f, g = 1.f;
+      if (t < K) {
+        const float A = -expf(gA);
+        const float av = ga + gdt;
+        const float sp = (av > 20.f) ? av : log1pf(expf(av));
+        g = expf(sp * A);
+        beta = 1.f / (1.f + expf(-gb));
+      }
+      sBG[(hv - hv0) * 2 * kKMax + t] = beta;
+      sBG[(hv - hv0) * 2 * kKMax + kKMax + t] = g;
+    }
+  };
+  gate_load(0);
+
+  // a1: conv of the head's q|k channels (thread cc < 2*DK owns one channel, its history, new
+  // history and snapshots; the snapshot stores leave from registers while the memory system is
+  // otherwise idle at the start of the step)
   if (tid < 2 * DK) {
     const int cc = tid;
     const int c = (cc < DK) ? kh * DK + cc : p.Hk * DK + kh * DK + (cc - DK);
@@ -151,7 +224,8 @@ __global__ void __launch_bounds__(kThreads) gdn_qk_prologue_kernel(const VerifyP
   }
   __syncthreads();
 
-  // a2: L2 norm of each of the 2K vectors (warp per vector); rows t >= K become zero
+  // a2: L2 norm of each of the 2K vectors (warp per vector, rows t >= K become zero), written
+  // straight into the swizzled table; a3 for up to 16 v-heads alongside
   for (int n = warp; n < kNCol; n += kWarps) {
     const int t = n % kKMax;
     float vals[DK / 32];
@@ -162,95 +236,132 @@ __global__ void __launch_bounds__(kThreads) gdn_qk_prologue_kernel(const VerifyP
       ss = fmaf(vals[m], vals[m], ss);
     }
     ss = warp_sum(ss);
-    const float inv = (t < K) ? 1.f / sqrtf(ss + p.l2_eps) : 0.f;
+    const float inv = (t < K) ? rsqrtf(ss + p.l2_eps) : 0.f;
+    if (lane == 0) sInv[n] = inv;
 #pragma unroll
-    for (int m = 0; m < DK / 32; ++m) sN[n * L::NSTRIDE + lane + 32 * m] = vals[m] * inv;
+    for (int m = 0; m < DK / 32; ++m) {
+      const int c = lane + 32 * m;
+      sT[wt_idx(c, n)] = vals[m] * inv;
+    }
+  }
+  gate_store(0);
+  __syncthreads();
+
+  // tables for the state kernel: [DK][32] in plain column order (un-swizzled while copying) and
+  // the token-major k^ [16][DK]
+  {
+    float* dst = p.ws.wt + head * DK * kNCol;
+    for (int f = tid; f < DK * kNCol; f += kThreads) dst[f] = sT[wt_idx(f / kNCol, f % kNCol)];
+    float* kn = p.ws.kn + head * kKMax * DK;
+    for (int f = tid; f < kKMax * DK; f += kThreads) kn[f] = sT[wt_idx(f % DK, f / DK)];
+  }
+
+  // Gram products from the raw rows: warp w takes rows 4w..4w+3 of [k; q] against the 16 k
+  // rows, eight at a time; lanes split the channels, a butterfly reduce-scatter leaves one sum
+  // per lane
+  {
+    constexpr int CPL = DK / 32;  // channels per lane
+    float rows[4][CPL];
+#pragma unroll
+    for (int m = 0; m < 4; ++m)
+#pragma unroll
+      for (int q = 0; q < CPL; ++q) rows[m][q] = sY[(4 * warp + m) * DK + CPL * lane + q];
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      float acc[32];
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        const int j = 8 * half + jj;
+        float kj[CPL];
+#pragma unroll
+        for (int q = 0; q < CPL; ++q) kj[q] = sY[j * DK + CPL * lane + q];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          float a = 0.f;
+#pragma unroll
+          for (int q = 0; q < CPL; ++q) a = fmaf(rows[m][q], kj[q], a);
+          acc[m * 8 + jj] = a;
+        }
+      }
+      warp_reduce_scatter(acc, lane);  // acc[0] = sum of value `lane` = (row lane / 8, column lane % 8)
+      const int n = 4 * warp + lane / 8, j = 8 * half + lane % 8;
+      const float v = acc[0] * sInv[n] * sInv[j];
+      if (n < kKMax)
+        sKK[n * kMStride + j] = v;
+      else
+        sKQ[(n - kKMax) * kMStride + j] = v;
+    }
   }
   __syncthreads();
 
-  // tables for the state kernel: swizzled [DK][32] and token-major k^ [16][DK]
-  const size_t head = size_t(b) * p.Hk + kh;
-  float* wt = p.ws.wt + head * DK * kNCol;
-  for (int f = tid; f < DK * kNCol; f += kThreads) {
-    const int c = f / kNCol;
-    const int col = (f % kNCol) ^ (c & 31);
-    wt[f] = sN[col * L::NSTRIDE + c];
-  }
-  float* kn = p.ws.kn + head * kKMax * DK;
-  for (int f = tid; f < kKMax * DK; f += kThreads) kn[f] = sN[(f / DK) * L::NSTRIDE + f % DK];
-
-  // Gram products of the window: KK[t][j] = k^_t . k^_j, KQ[t][j] = k^_j . q^_t
-  {
-    const int t = tid >> 4, j = tid & 15;
-    const float* kt = sN + t * L::NSTRIDE;
-    const float* kj = sN + j * L::NSTRIDE;
-    const float* qt = sN + (kKMax + t) * L::NSTRIDE;
-    float kk = 0.f, kq = 0.f;
-#pragma unroll 8
-    for (int c = 0; c < DK; ++c) {
-      kk = fmaf(kt[c], kj[c], kk);
-      kq = fmaf(qt[c], kj[c], kq);
+  // per-v-head gate blocks: M = D * (k^.k^) strictly lower, N = q_scale * D * (k^.q^) lower,
+  // Gamma, beta, g; D[t][j] = prod_{j<m<=t} g_m as a masked product over registers
+  const int t = tid >> 4, j = tid & 15;
+  const float kk = sKK[t * kMStride + j];
+  const float kq = sKQ[t * kMStride + j];
+  for (int hv0 = 0; hv0 < r; hv0 += 16) {
+    if (hv0 > 0) {
+      __syncthreads();
+      gate_load(hv0);
+      gate_store(hv0);
+      __syncthreads();
     }
-    sKK[t * kMStride + j] = kk;
-    sKQ[t * kMStride + j] = kq;
-  }
-
-  // a3 and the per-v-head gate blocks
-  for (int hv = 0; hv < r; ++hv) {
-    const int h = kh * r + hv;
-    __syncthreads();  // Gram ready (first pass); previous head's beta/g consumed
-    if (tid < kKMax) {
-      float beta = 0.f, g = 1.f;
-      if (tid < K) {
-        const float A = -expf(p.A_log[h]);
-        const size_t gi = (size_t(b) * K + tid) * p.Hv + h;
-        const float av = bf16_to_f32(p.a[gi]) + p.dt_bias[h];
-        const float sp = (av > 20.f) ? av : log1pf(expf(av));
-        g = expf(sp * A);
-        beta = 1.f / (1.f + expf(-bf16_to_f32(p.b[gi])));
+    for (int hv = hv0; hv < min(r, hv0 + 16); ++hv) {
+      const float* bg = sBG + (hv - hv0) * 2 * kKMax;
+      float g[kKMax];
+#pragma unroll
+      for (int m = 0; m < kKMax; m += 4) {
+        const float4 v = *reinterpret_cast<const float4*>(bg + kKMax + m);
+        g[m] = v.x;
+        g[m + 1] = v.y;
+        g[m + 2] = v.z;
+        g[m + 3] = v.w;
       }
-      sBeta[tid] = beta;
-      sG[tid] = g;
+      float d = 1.f;
+#pragma unroll
+      for (int m = 1; m < kKMax; ++m) d *= (m > j && m <= t) ? g[m] : 1.f;
+      float* gate = p.ws.gate + (size_t(b) * p.Hv + kh * r + hv) * kGateFloats;
+      gate[t * kMStride + j] = (j < t) ? d * kk : 0.f;
+      gate[kGateOffN + t * kMStride + j] = (j <= t) ? p.q_scale * d * kq : 0.f;
+      if (j == 0) gate[kGateOffGam + t] = d * g[0];
+      if (tid < kKMax) {
+        gate[tid * kMStride + kKMax] = 0.f;
+        gate[kGateOffN + tid * kMStride + kKMax] = 0.f;
+        gate[kGateOffBeta + tid] = bg[tid];
+        gate[kGateOffG + tid] = bg[kKMax + tid];
+      }
+      if (tid < kGateFloats - (kGateOffGam + kKMax)) gate[kGateOffGam + kKMax + tid] = 0.f;
     }
-    __syncthreads();
-    float* gate = p.ws.gate + (size_t(b) * p.Hv + h) * kGateFloats;
-    const int t = tid >> 4, j = tid & 15;
-    float d = 1.f;
-    for (int m = j + 1; m <= t; ++m) d *= sG[m];
-    gate[t * kMStride + j] = (j < t) ? d * sKK[t * kMStride + j] : 0.f;
-    gate[kGateOffN + t * kMStride + j] = (j <= t) ? p.q_scale * d * sKQ[t * kMStride + j] : 0.f;
-    if (j == 0) gate[kGateOffGam + t] = d * sG[0];
-    if (tid < kKMax) {
-      gate[tid * kMStride + kKMax] = 0.f;
-      gate[kGateOffN + tid * kMStride + kKMax] = 0.f;
-      gate[kGateOffBeta + tid] = sBeta[tid];
-      gate[kGateOffG + tid] = sG[tid];
-    }
-    if (tid < kGateFloats - (kGateOffGam + kKMax)) gate[kGateOffGam + kKMax + tid] = 0.f;
   }
+  // the state kernel's independent work (S0 copy, v-channel conv) starts as this grid finishes;
+  // earlier starts only made the two grids contend for the SMs (measured)
+  griddep_launch_dependents();
 }
 
 // ------------------------------------------------------------------------------------------
 // Kernel 2: per (sequence, v-head, 32-row tile) state stream.
 template <int DK>
 struct StreamLayout {
-  static constexpr int PSTRIDE = kNCol + 1;
+  static constexpr int PSTRIDE = kNCol + 4;                    // 16-byte rows
+  static constexpr int RSTRIDE = kKMax + 1;
   static constexpr int OFF_S0 = 0;                               // [32][DK]      bulk copy
   static constexpr int OFF_WT = OFF_S0 + kRows * DK;             // [DK][32]      bulk copy
-  static constexpr int OFF_KN = OFF_WT + DK * kNCol;             // [16][DK]      bulk copy
-  static constexpr int OFF_GATE = OFF_KN + kKMax * DK;           // gate block    bulk copy
-  static constexpr int OFF_V = OFF_GATE + kGateFloats;           // [warp][16][4] v conv outputs
+  static constexpr int OFF_GATE = OFF_WT + DK * kNCol;           // gate block    bulk copy
+  static constexpr int OFF_KN = OFF_GATE + kGateFloats;          // [16][DK] k^ token-major, bulk copy
+  static constexpr int OFF_V = OFF_KN + kKMax * DK;              // [warp][16][4] v conv outputs
   static constexpr int OFF_U = OFF_V + kWarps * kKMax * kRowsPerWarp;  // [warp][16][4] u
-  static constexpr int OFF_P = OFF_U + kWarps * kKMax * kRowsPerWarp;  // [32][33] S0 [k^ | q^]
-  static constexpr int OFF_BAR = (OFF_P + kRows * PSTRIDE + 1) & ~1;
+  static constexpr int OFF_P = OFF_U + kWarps * kKMax * kRowsPerWarp;  // [32][PSTRIDE] S0 [k^ | q^]
+  static constexpr int OFF_R = OFF_P + kRows * PSTRIDE;                // [32][RSTRIDE] rhs
+  static constexpr int OFF_BAR = (OFF_R + kRows * RSTRIDE + 1) & ~1;  // 8-byte aligned mbarrier
   static constexpr int FLOATS = OFF_BAR + 2;
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
   static constexpr uint32_t S0_BYTES = kRows * DK * 4;
   static constexpr uint32_t WT_BYTES = DK * kNCol * 4;
-  static constexpr uint32_t KN_BYTES = kKMax * DK * 4;
   static constexpr uint32_t GATE_BYTES = kGateFloats * 4;
-  static_assert(S0_BYTES % 16 == 0 && WT_BYTES % 16 == 0 && KN_BYTES % 16 == 0 && GATE_BYTES % 16 == 0, "");
-  static_assert(OFF_WT % 4 == 0 && OFF_KN % 4 == 0 && OFF_GATE % 4 == 0, "bulk destinations 16-byte aligned");
+  static constexpr uint32_t KN_BYTES = kKMax * DK * 4;
+  static_assert(S0_BYTES % 16 == 0 && WT_BYTES % 16 == 0 && GATE_BYTES % 16 == 0 && KN_BYTES % 16 == 0, "");
+  static_assert(OFF_WT % 4 == 0 && OFF_GATE % 4 == 0 && OFF_KN % 4 == 0 && OFF_P % 4 == 0,
+                "bulk destinations and float4 rows 16-byte aligned");
 };
 
 template <int DK, int DV>
@@ -279,13 +390,24 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::KN_BYTES + L::GATE_BYTES);
-    bulk_load(sS0, p.state_in + tile_off, L::S0_BYTES, bar);
+  }
+  __syncthreads();  // the barrier is initialised before any thread polls it
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES);
+    // S0: the previous final state, or (rollback applied on read) the accepted intermediate or
+    // the pre-window snapshot of the previous window
+    const int Lp = prev_accept(p, b, blockIdx.x == 0);
+    const float* s0 = p.state_in + tile_off;
+    if (Lp == 0)
+      s0 = p.state_snap_prev + tile_off;
+    else if (Lp > 0 && Lp < K)
+      s0 = p.state_inter_prev + (size_t(b) * (K - 1) + (Lp - 1)) * size_t(p.Hv) * DV * DK + (size_t(h) * DV + r0) * DK;
+    bulk_load(sS0, s0, L::S0_BYTES, bar);
     griddep_wait();  // the prologue grid has finished and its tables are visible
     const size_t head = size_t(b) * p.Hk + kh;
     bulk_load(sWT, p.ws.wt + head * DK * kNCol, L::WT_BYTES, bar);
-    bulk_load(sKn, p.ws.kn + head * kKMax * DK, L::KN_BYTES, bar);
     bulk_load(sGate, p.ws.gate + (size_t(b) * p.Hv + h) * kGateFloats, L::GATE_BYTES, bar);
+    bulk_load(sKn, p.ws.kn + head * kKMax * DK, L::KN_BYTES, bar);
   }
 
   // a1 for this CTA's v-channels: lanes 4..7 of warp w convolve rows 4w..4w+3
@@ -296,9 +418,11 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
 #pragma unroll
     for (int t = 0; t < kKMax; ++t) sV[t * kRowsPerWarp + (lane - 4)] = y[t];
   }
+
   __syncwarp();
 
-  // S0 and the tables must have landed (bounded wait, warp-uniform outcome)
+  // S0 and the tables must have landed (bounded wait, warp-uniform outcome; no CTA-wide barrier
+  // follows, so each warp proceeds on its own)
   int ok = 1;
   if (lane == 0) ok = mbar_wait_bounded(bar, 0) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -314,76 +438,88 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   const float* gG = sGate + kGateOffG;
   const float* gGam = sGate + kGateOffGam;
   float* sP = sm + L::OFF_P;
+  float* sR = sm + L::OFF_R;
   const int row0 = warp * kRowsPerWarp;
+  const int m = lane >> 3;   // row of this warp handled by this lane in the phases below
+  const int cg = lane & 7;   // column group (P) / token (outputs)
 
-  // P = S0 [k^ | q^] for this warp's rows, lane = column
+  // P = S0 [k^ | q^]: lane (m, cg) computes columns 4cg..4cg+3 of row row0+m; for the k^
+  // columns the right-hand side rhs_j = v_j - Gamma_j (S0 k^_j) right away
   {
-    float acc[kRowsPerWarp];
-#pragma unroll
-    for (int m = 0; m < kRowsPerWarp; ++m) acc[m] = 0.f;
+    float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+    const float* srow = sS0 + (row0 + m) * DK;
+    const float* wcol = sWT + 4 * cg;
 #pragma unroll 4
     for (int c = 0; c < DK; c += 4) {
-      float wv[4];
+      const float4 sv = *reinterpret_cast<const float4*>(srow + c);
+      const float sc[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) wv[q] = sWT[wt_idx(c + q, lane)];
-#pragma unroll
-      for (int m = 0; m < kRowsPerWarp; ++m) {
-        const float4 s = *reinterpret_cast<const float4*>(sS0 + (row0 + m) * DK + c);
-        acc[m] = fmaf(s.x, wv[0], fmaf(s.y, wv[1], fmaf(s.z, wv[2], fmaf(s.w, wv[3], acc[m]))));
+      for (int q = 0; q < 4; ++q) {
+        const float4 w = *reinterpret_cast<const float4*>(wcol + (c + q) * kNCol);
+        const float2 ss = make_float2(sc[q], sc[q]);
+        acc01 = __ffma2_rn(ss, make_float2(w.x, w.y), acc01);
+        acc23 = __ffma2_rn(ss, make_float2(w.z, w.w), acc23);
       }
     }
+    const float pv[4] = {acc01.x, acc01.y, acc23.x, acc23.y};
+    *reinterpret_cast<float4*>(sP + (row0 + m) * L::PSTRIDE + 4 * cg) = make_float4(pv[0], pv[1], pv[2], pv[3]);
+    if (cg < 4) {
 #pragma unroll
-    for (int m = 0; m < kRowsPerWarp; ++m) sP[(row0 + m) * L::PSTRIDE + lane] = acc[m];
+      for (int i = 0; i < 4; ++i) {
+        const int jj = 4 * cg + i;
+        sR[(row0 + m) * L::RSTRIDE + jj] = fmaf(-gGam[jj], pv[i], sV[jj * kRowsPerWarp + m]);
+      }
+    }
   }
   __syncwarp();
 
-  // forward substitution for u, lanes 0..3 (one row each)
+  // forward substitution u_t = beta_t (rhs_t - sum_{j<t} M[t][j] u_j), lanes 0..3 (one row each)
   if (lane < kRowsPerWarp) {
-    const float* P = sP + (row0 + lane) * L::PSTRIDE;
+    const float* rh = sR + (row0 + lane) * L::RSTRIDE;
     float u[kKMax];
 #pragma unroll
-    for (int t = 0; t < kKMax; ++t) {
-      u[t] = 0.f;
-      if (t < K) {
-        float acc = fmaf(-gGam[t], P[t], sV[t * kRowsPerWarp + lane]);
+    for (int tt = 0; tt < kKMax; ++tt) {
+      u[tt] = 0.f;
+      if (tt < K) {
+        float acc = rh[tt];
 #pragma unroll
-        for (int j = 0; j < t; ++j) acc = fmaf(-gM[t * kMStride + j], u[j], acc);
-        u[t] = gBeta[t] * acc;
-        sU[t * kRowsPerWarp + lane] = u[t];
+        for (int jj = 0; jj < tt; ++jj) acc = fmaf(-gM[tt * kMStride + jj], u[jj], acc);
+        u[tt] = gBeta[tt] * acc;
+        sU[tt * kRowsPerWarp + lane] = u[tt];
       }
     }
   }
   __syncwarp();
 
-  // outputs: lane -> (row m = lane / 8, tokens t0 and t0 + 8)
-  {
-    const int m = lane >> 3;
-    const float* P = sP + (row0 + m) * L::PSTRIDE;
+  // outputs o_t = q_scale Gamma_t Pq_t + sum_{j<=t} N[t][j] u_j: lane -> (row m, tokens cg, cg + 8)
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int t = (lane & 7) + 8 * half;
-      if (t < K) {
-        float o = p.q_scale * gGam[t] * P[kKMax + t];
-        for (int j = 0; j <= t; ++j) o = fmaf(gN[t * kMStride + j], sU[j * kRowsPerWarp + m], o);
-        const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
-        if (p.out_f32)
-          static_cast<float*>(p.out)[oi] = o;
-        else
-          static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(o);
-      }
+  for (int half = 0; half < 2; ++half) {
+    const int t = cg + 8 * half;
+    if (t < K) {
+      float o = p.q_scale * gGam[t] * sP[(row0 + m) * L::PSTRIDE + kKMax + t];
+      for (int jj = 0; jj <= t; ++jj) o = fmaf(gN[t * kMStride + jj], sU[jj * kRowsPerWarp + m], o);
+      const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
+      if (p.out_f32)
+        static_cast<float*>(p.out)[oi] = o;
+      else
+        static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(o);
     }
   }
+  __syncwarp();
 
   // stream the K states from registers: lane owns DK/32 float4 of the warp's 4 rows
   constexpr int F4 = DK / 32;
   constexpr int C4 = DK / 4;
+  // float4 q of this lane sits in row rowq[q] of the warp's rows, column c4 (row and column are
+  // compile-time constants per q when a row spans the whole warp)
+  static_assert(C4 == 32 || C4 == 16, "dk = 128 or 64");
+  const int row_lane = (C4 == 32) ? 0 : lane / C4;
   int rowq[F4];
   float4 s[F4];
-  const int c4 = lane % C4;
+  const int c4 = (C4 == 32) ? lane : lane % C4;
 #pragma unroll
   for (int q = 0; q < F4; ++q) {
-    const int f = lane + 32 * q;
-    rowq[q] = f / C4;
+    rowq[q] = q * (32 / C4) + row_lane;
     s[q] = *reinterpret_cast<const float4*>(sS0 + (row0 + rowq[q]) * DK + 4 * c4);
   }
   const size_t inter_stride = size_t(p.Hv) * DV * DK;
@@ -397,10 +533,12 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
 #pragma unroll
     for (int q = 0; q < F4; ++q) {
       const float u = sU[t * kRowsPerWarp + rowq[q]];
-      s[q].x = fmaf(u, kv.x, g * s[q].x);
-      s[q].y = fmaf(u, kv.y, g * s[q].y);
-      s[q].z = fmaf(u, kv.z, g * s[q].z);
-      s[q].w = fmaf(u, kv.w, g * s[q].w);
+      {  // s = g s + u k, two lanes of f32 per instruction
+        const float2 gg = make_float2(g, g), uu = make_float2(u, u);
+        const float2 lo = __ffma2_rn(uu, make_float2(kv.x, kv.y), __fmul2_rn(gg, make_float2(s[q].x, s[q].y)));
+        const float2 hi = __ffma2_rn(uu, make_float2(kv.z, kv.w), __fmul2_rn(gg, make_float2(s[q].z, s[q].w)));
+        s[q] = make_float4(lo.x, lo.y, hi.x, hi.y);
+      }
       float4* d4 = reinterpret_cast<float4*>(dst + size_t(rowq[q]) * DK);
       if (t == K - 1)
         *d4 = s[q];

@@ -109,3 +109,14 @@ class GdnLayerState:
         """One verify + rollback round on the loaded window and accept lengths."""
         self.verify(stream)
         self.rollback(stream)
+
+    def verify_resume(self, accept_prev, stream=None) -> None:
+        """Verify the loaded window after applying the previous window's accept lengths on read
+        (gdn_verify_resume, in place, no snapshot: lengths must be >= 1).  The state buffers then
+        hold this window's final state and intermediates, as after `verify`."""
+        if self.keep_snapshot:
+            raise ValueError("verify_resume works in place; create the state without keep_snapshot")
+        S, CS = self.states[0], self.conv_states[0]
+        gdn.gdn_verify_resume(self.dims, accept_prev, self.x, self.a, self.b, self.A_log, self.dt_bias, self.conv_w,
+                              CS, self.conv_inter, None, CS, self.conv_inter, S, self.state_inter, None, S,
+                              self.state_inter, self.out, self.workspace, stream)

@@ -55,7 +55,7 @@ def test_static_scratch_matches_workspace_entry_point():
 
 def test_static_scratch_rejects_oversized_dims():
     lib = gdn.load_library()
-    dims = gdn.make_dims(B=64, K=16, Hk=16, Hv=32, dk=128, dv=128)   # needs 30 MB of scratch
+    dims = gdn.make_dims(B=64, K=16, Hk=16, Hv=32, dk=128, dv=128)   # needs 30.0 MB of scratch
     status = lib.gdn_verify_step_static_scratch(ctypes.byref(dims), *([ctypes.c_void_p(1 << 32)] * 13), None)
     assert status == gdn.GDN_ERR_UNSUPPORTED
     assert "static scratch" in gdn.last_error()
