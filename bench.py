@@ -200,7 +200,7 @@ def run_gdn(args):
     from speculative_decode_verify_gdn_gb300 import gdn
     from speculative_decode_verify_gdn_gb300.build import build_library, kernel_source_digest
     from speculative_decode_verify_gdn_gb300.runtime import GdnLayerState
-    from speculative_decode_verify_gdn_gb300.synth import WORKLOADS, Gen, make_layer, make_round
+    from speculative_decode_verify_gdn_gb300.synth import WORKLOADS, Gen, make_layer, make_round, make_tree
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -293,6 +293,32 @@ def run_gdn(args):
     if gdn.gdn_device_status(clear=True):
         raise RuntimeError("device status flags after the resume steps")
 
+    # token-tree verify (gdn_verify_tree) on the same shapes: one seeded tree per sequence in
+    # which each node continues the previous one with probability 1/2, else branches
+    parent = torch.from_numpy(make_tree(Gen(w.seed + 77), d.B, d.K, 0.5)).to(dev)
+
+    def tree_step(i):
+        j = i % n_in
+        gdn.gdn_verify_tree(dims, parent, xs[j], as_[j], bs[j], st.A_log, st.dt_bias, st.conv_w, CS, CS, CI, S0, S0,
+                            SI, OUT, WS, stream)
+
+    for i in range(args.warmup):
+        tree_step(i)
+    barrier()
+    r0.record(stream)
+    n_tree = max(3, args.steps // 5)
+    for i in range(n_tree):
+        tree_step(i)
+    r1.record(stream)
+    barrier()
+    tms = max_over_ranks(r0.elapsed_time(r1), world, dev)
+    tree = {"value": job_throughput(d.B * d.K * n_tree, world, tms), "unit": "tree nodes/s",
+            "ms_per_step": tms / n_tree, "steps": n_tree, "gpu_launches": 2 * n_tree,
+            "hbm_frac": verify_bytes(d, out_bytes=2) / (tms / n_tree * 1e-3) / 1e9 / measured_peak_gbs()[0],
+            "what": "gdn_verify_tree per step, B=32 trees of 16 nodes (chain continuation 1/2)"}
+    if gdn.gdn_device_status(clear=True):
+        raise RuntimeError("device status flags after the tree steps")
+
     # e2e: inputs from pinned host memory and the output back, inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -354,6 +380,7 @@ def run_gdn(args):
         "clocks": clocks.summary(),
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "zero_copy_rollback": resume,
+        "tree_verify": tree,
     }
     if world > 1:
         dist.barrier()

@@ -60,6 +60,7 @@ typedef enum {
 #define GDN_DEVERR_TIMEOUT 1u      /* a bounded wait in a kernel gave up; its results are invalid */
 #define GDN_DEVERR_ACCEPT_RANGE 2u /* rollback saw an accept length outside 0..K; that sequence was left as is */
 #define GDN_DEVERR_NO_SNAPSHOT 4u  /* rollback saw accept length 0 with no snapshot; that sequence was left as is */
+#define GDN_DEVERR_TREE_PARENT 8u  /* a token tree had a parent outside -1..t-1; it was read as -1 */
 
 typedef struct {
   int32_t B;       /* sequences */
@@ -151,6 +152,28 @@ gdn_status gdn_verify_resume(const gdn_dims* dims, const int32_t* accept_len_pre
                              const float* state_in, const float* state_inter_prev, const float* state_snapshot_prev,
                              float* state_out, float* state_inter, void* out, void* workspace,
                              uint64_t workspace_bytes, gdn_stream_t stream);
+
+/*
+ * a1..a4 over a token tree instead of a chain (DDTree-style verify; lucebox #637,
+ * review of ggml.c: ggml_ssm_conv_tree, the tree variant of the conv step).
+ *   parent_dev  [B, K] int32 on the device: parent[b][t] in -1..t-1 (nodes in
+ *               topological order; -1 = a child of the committed state).
+ * Every node sees the sequence along its root-to-node path: its conv window is
+ * the W-1 newest rows of [history; x of the path nodes above it], and its state
+ * is the rule applied to its parent's state (conv_state_in / state_in for -1).
+ * Node t's state and history go where token t's go in gdn_verify_step
+ * (state_inter[b][t] for t < K-1, state_out / conv_state_out for node K-1,
+ * conv_inter[b][t]), so gdn_rollback with accept_len = n + 1 rolls a sequence
+ * back to accepted node n (0 for none).  A chain (parent[t] = t-1) gives
+ * gdn_verify_step's results.  A parent outside -1..t-1 is read as -1 and sets
+ * GDN_DEVERR_TREE_PARENT.  Other arguments, aliasing and workspace as
+ * gdn_verify_step.
+ */
+gdn_status gdn_verify_tree(const gdn_dims* dims, const int32_t* parent_dev, const uint16_t* x, const uint16_t* a,
+                           const uint16_t* b, const float* A_log, const float* dt_bias, const float* conv_w,
+                           const float* conv_state_in, float* conv_state_out, float* conv_inter,
+                           const float* state_in, float* state_out, float* state_inter, void* out,
+                           void* workspace, uint64_t workspace_bytes, gdn_stream_t stream);
 
 /*
  * Bytes of workspace gdn_verify_step needs for `dims`:

@@ -30,6 +30,9 @@ time, in the order the pages give it:
       Qwen3.8 Flash runtime fixes", commits on recurrent snapshot planes and on
       restoring full checkpoints)
 
+and the same step over a token tree (DDTree-style window: each node continues its
+parent's state and conv history; lucebox #637, ``ggml_ssm_conv_tree``).
+
 Readings taken where the pages are silent (each is also listed in the design
 notes): taps are a cross-correlation with w[c, W-1] on the current token; no
 conv bias; the L2 norm is x / sqrt(sum x^2 + eps); v-head h reads q/k head
@@ -211,3 +214,76 @@ def rollback(accept_len, state0, states, conv_state0, conv_inter):
             st[bi] = states[bi, L - 1]
             cs[bi] = conv_inter[bi, L - 1]
     return st, cs
+
+
+def tree_verify_step(dims, parent, x, a, b, A_log, dt_bias, conv_w, conv_state, state,
+                     q_scale: float = 1.0, l2_eps: float = 1e-6):
+    """Verify of a token tree (DDTree-style window; lucebox #637, review of ggml.c:
+    ``ggml_ssm_conv_tree``, the tree variant of the conv step).
+
+    parent [B, K]: parent[b][t] in -1..t-1 (-1: a child of the committed state), nodes
+    in topological order.  Every node sees the sequence along its root-to-node path:
+      conv window of node t = the W-1 newest rows of [history; x of the path nodes up to
+      its parent], then x_t;
+      state S_t = rule(S_parent) (S_{-1} = the state before the window);
+      o_t = q_scale * S_t q_t.
+    Returns the same dict as verify_step, with states[:, t] the state after node t,
+    conv_inter[:, t] the history after node t, and the *_out entries those of node K-1.
+    """
+    x = np.asarray(x, np.float64)
+    w = np.asarray(conv_w, np.float64)
+    hist = np.asarray(conv_state, np.float64)
+    parent = np.asarray(parent)
+    B, K, C = x.shape
+    W = w.shape[1]
+    y = np.empty((B, K, C))
+    conv_inter = np.empty((B, K, W - 1, C))
+    for bi in range(B):
+        for t in range(K):
+            p = int(parent[bi, t])
+            if not -1 <= p < t:
+                raise ValueError(f"parent[{bi}][{t}] = {p} is not in -1..{t - 1}")
+            prev = hist[bi] if p < 0 else conv_inter[bi, p]       # history after the parent
+            win = np.concatenate([prev, x[bi, t:t + 1]], axis=0)  # W rows, oldest first
+            y[bi, t] = silu(np.sum(w.T * win, axis=0))
+            conv_inter[bi, t] = win[1:]
+    q, k, v = split_qkv(y, dims.Hk, dims.Hv, dims.dk, dims.dv)
+    qn = l2_normalize(q, l2_eps)
+    kn = l2_normalize(k, l2_eps)
+    beta, g = raw_gates(a, b, A_log, dt_bias)
+    Hk, Hv = dims.Hk, dims.Hv
+    kh = np.arange(Hv) // (Hv // Hk)
+    S0 = np.asarray(state, np.float64)
+    states = np.empty((B, K) + S0.shape[1:])
+    o = np.empty((B, K, Hv, dims.dv))
+    for bi in range(B):
+        for t in range(K):
+            p = int(parent[bi, t])
+            S = S0[bi] if p < 0 else states[bi, p]
+            k_t = kn[bi, t, kh]
+            q_t = qn[bi, t, kh]
+            g_t = g[bi, t][:, None, None]
+            pk = np.einsum("hij,hj->hi", S, k_t)
+            delta = beta[bi, t][:, None] * (v[bi, t] - g[bi, t][:, None] * pk)
+            St = g_t * S + delta[:, :, None] * k_t[:, None, :]
+            states[bi, t] = St
+            o[bi, t] = q_scale * np.einsum("hij,hj->hi", St, q_t)
+    return {
+        "out": o,
+        "states": states,
+        "state_out": states[:, -1],
+        "state_inter": states[:, :-1],
+        "conv_inter": conv_inter,
+        "conv_state_out": conv_inter[:, -1],
+        "y": y,
+    }
+
+
+def tree_path(parent_row, t):
+    """Nodes on the root-to-node path of node t, root first."""
+    path = []
+    n = int(t)
+    while n >= 0:
+        path.append(n)
+        n = int(parent_row[n])
+    return path[::-1]

@@ -59,6 +59,8 @@ struct VerifyParams {
   const float* conv_inter_prev;
   const float* state_snap_prev;  // may be null (then L == 0 is an error)
   const float* conv_snap_prev;
+  // Token tree (gdn_verify_tree; null for a chain window): parent[b][t] in -1..t-1.
+  const int32_t* parent;
   uint32_t* err;       // device status word
   int B, K, Hk, Hv, dk, dv, C;
   float q_scale, l2_eps;

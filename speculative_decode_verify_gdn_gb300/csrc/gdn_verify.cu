@@ -93,9 +93,81 @@ __device__ __forceinline__ const float* history_src(const VerifyParams& p, int b
   return p.conv_inter_prev + (size_t(b) * p.K + (L - 1)) * 3 * C + c;
 }
 
-// Conv + SiLU of one channel over the window; writes the channel's K history snapshots (if
-// requested) and its new history.  y[t] receives the outputs for t < K.
-__device__ __forceinline__ void conv_channel(const VerifyParams& p, int b, int c, float (&y)[kKMax]) {
+// Token-tree window (gdn_verify_tree): per node t its parent, the three window rows before x_t
+// as indices into [history row 0, 1, 2, x_0 .. x_{K-1}], and the bit set of the nodes on its
+// root-to-node path.  Built by one thread; a parent outside -1..t-1 reads as -1 and is flagged.
+struct TreeTable {
+  int parent[kKMax];
+  int src[kKMax][3];
+  unsigned path[kKMax];
+};
+
+__device__ __forceinline__ void build_tree(const VerifyParams& p, int b, TreeTable* tt, bool report) {
+  for (int t = 0; t < p.K; ++t) {
+    int par = p.parent[size_t(b) * p.K + t];
+    if (par < -1 || par >= t) {
+      if (report) atomicOr(p.err, kDevErrTreeParent);
+      par = -1;
+    }
+    tt->parent[t] = par;
+    if (par < 0) {
+      tt->src[t][0] = 0;
+      tt->src[t][1] = 1;
+      tt->src[t][2] = 2;
+      tt->path[t] = 1u << t;
+    } else {
+      tt->src[t][0] = tt->src[par][1];
+      tt->src[t][1] = tt->src[par][2];
+      tt->src[t][2] = 3 + par;
+      tt->path[t] = tt->path[par] | (1u << t);
+    }
+  }
+}
+
+// Conv + SiLU of one channel over the window (a chain of K tokens, or a token tree when kTree);
+// writes the channel's K history snapshots and its new history (that after token / node K-1).
+// y[t] receives the outputs for t < K.
+template <bool kTree>
+__device__ __forceinline__ void conv_channel(const VerifyParams& p, int b, int c, const TreeTable* tt,
+                                             float (&y)[kKMax]) {
+  if constexpr (kTree) {
+    const int C = p.C;
+    const int K = p.K;
+    const float4 w = *reinterpret_cast<const float4*>(p.conv_w + size_t(c) * kConvW);
+    const float* hin = p.conv_state_in + size_t(b) * 3 * C + c;
+    float vals[3 + kKMax];  // [history rows 0..2, x_0 .. x_{K-1}]
+    vals[0] = hin[0];
+    vals[1] = hin[C];
+    vals[2] = hin[2 * C];
+    const uint16_t* xp = p.x + size_t(b) * K * C + c;
+#pragma unroll
+    for (int t = 0; t < kKMax; ++t) vals[3 + t] = (t < K) ? bf16_to_f32(xp[size_t(t) * C]) : 0.f;
+    float* ci = p.conv_inter ? p.conv_inter + size_t(b) * K * 3 * C + c : nullptr;
+    float n0 = 0.f, n1 = 0.f, n2 = 0.f;
+#pragma unroll
+    for (int t = 0; t < kKMax; ++t) {
+      y[t] = 0.f;
+      if (t < K) {
+        const float w0 = vals[tt->src[t][0]], w1 = vals[tt->src[t][1]], w2 = vals[tt->src[t][2]];
+        const float xt = vals[3 + t];
+        y[t] = silu(fmaf(w.w, xt, fmaf(w.z, w2, fmaf(w.y, w1, w.x * w0))));
+        n0 = w1;
+        n1 = w2;
+        n2 = xt;
+        if (ci) {
+          ci[size_t(3 * t + 0) * C] = n0;
+          ci[size_t(3 * t + 1) * C] = n1;
+          ci[size_t(3 * t + 2) * C] = n2;
+        }
+      }
+    }
+    float* hout = p.conv_state_out + size_t(b) * 3 * C + c;
+    hout[0] = n0;
+    hout[C] = n1;
+    hout[2 * C] = n2;
+    return;
+  }
+  (void)tt;
   const int C = p.C;
   const int K = p.K;
   const float4 w = *reinterpret_cast<const float4*>(p.conv_w + size_t(c) * kConvW);
@@ -138,7 +210,8 @@ struct PrologueLayout {
   static constexpr int OFF_KK = OFF_INV + kNCol;            // k^_t . k^_j  [16][17]
   static constexpr int OFF_KQ = OFF_KK + kKMax * kMStride;  // k^_j . q^_t  [16][17]
   static constexpr int OFF_BG = OFF_KQ + kKMax * kMStride;  // beta, g of up to 16 v-heads [16][2][16]
-  static constexpr int FLOATS = OFF_BG + 16 * 2 * kKMax;
+  static constexpr int OFF_TREE = OFF_BG + 16 * 2 * kKMax;  // TreeTable (token trees only)
+  static constexpr int FLOATS = OFF_TREE + int(sizeof(TreeTable) / 4);
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
   static_assert(OFF_T % 4 == 0 && OFF_BG % 4 == 0, "float4 access");
 };
@@ -158,7 +231,7 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[32], int lane) {
   }
 }
 
-template <int DK>
+template <int DK, bool kTree>
 __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const VerifyParams p) {
   using L = PrologueLayout<DK>;
   extern __shared__ __align__(128) float sm[];
@@ -208,6 +281,11 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
     }
   };
   gate_load(0);
+  TreeTable* tree = reinterpret_cast<TreeTable*>(sm + L::OFF_TREE);
+  if constexpr (kTree) {
+    if (tid == 0) build_tree(p, b, tree, kh == 0);
+    __syncthreads();
+  }
 
   // a1: conv of the head's q|k channels (thread cc < 2*DK owns one channel, its history, new
   // history and snapshots; the snapshot stores leave from registers while the memory system is
@@ -216,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
     const int cc = tid;
     const int c = (cc < DK) ? kh * DK + cc : p.Hk * DK + kh * DK + (cc - DK);
     float y[kKMax];
-    conv_channel(p, b, c, y);
+    conv_channel<kTree>(p, b, c, tree, y);
     const int n0 = (cc < DK) ? kKMax : 0;  // q rows 16..31, k rows 0..15
     const int col = cc % DK;
 #pragma unroll
@@ -317,13 +395,29 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
         g[m + 2] = v.z;
         g[m + 3] = v.w;
       }
+      // chain: j < t are the earlier tokens and the path below j is j+1..t; tree: j must lie on
+      // t's root-to-node path, and the nodes below it are t's path minus j's (same products,
+      // same order, so a chain-shaped tree gives the chain's numbers bit for bit)
+      bool below = j < t, on_path = j <= t;
+      unsigned down = 0;
+      int root = 0;
+      if constexpr (kTree) {
+        const unsigned pt = tree->path[t], pj = tree->path[j];
+        on_path = j <= t && ((pt >> j) & 1u);
+        below = on_path && j < t;
+        down = pt & ~pj;
+        root = __ffs(pt) - 1;
+      }
       float d = 1.f;
 #pragma unroll
-      for (int m = 1; m < kKMax; ++m) d *= (m > j && m <= t) ? g[m] : 1.f;
+      for (int m = 1; m < kKMax; ++m) {
+        const bool in = kTree ? ((down >> m) & 1u) : (m > j && m <= t);
+        d *= in ? g[m] : 1.f;
+      }
       float* gate = p.ws.gate + (size_t(b) * p.Hv + kh * r + hv) * kGateFloats;
-      gate[t * kMStride + j] = (j < t) ? d * kk : 0.f;
-      gate[kGateOffN + t * kMStride + j] = (j <= t) ? p.q_scale * d * kq : 0.f;
-      if (j == 0) gate[kGateOffGam + t] = d * g[0];
+      gate[t * kMStride + j] = below ? d * kk : 0.f;
+      gate[kGateOffN + t * kMStride + j] = on_path ? p.q_scale * d * kq : 0.f;
+      if (j == root) gate[kGateOffGam + t] = d * g[root];
       if (tid < kKMax) {
         gate[tid * kMStride + kKMax] = 0.f;
         gate[kGateOffN + tid * kMStride + kKMax] = 0.f;
@@ -352,7 +446,8 @@ struct StreamLayout {
   static constexpr int OFF_U = OFF_V + kWarps * kKMax * kRowsPerWarp;  // [warp][16][4] u
   static constexpr int OFF_P = OFF_U + kWarps * kKMax * kRowsPerWarp;  // [32][PSTRIDE] S0 [k^ | q^]
   static constexpr int OFF_R = OFF_P + kRows * PSTRIDE;                // [32][RSTRIDE] rhs
-  static constexpr int OFF_BAR = (OFF_R + kRows * RSTRIDE + 1) & ~1;  // 8-byte aligned mbarrier
+  static constexpr int OFF_TREE = OFF_R + kRows * RSTRIDE;              // TreeTable (token trees only)
+  static constexpr int OFF_BAR = (OFF_TREE + int(sizeof(TreeTable) / 4) + 1) & ~1;  // 8-byte aligned mbarrier
   static constexpr int FLOATS = OFF_BAR + 2;
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
   static constexpr uint32_t S0_BYTES = kRows * DK * 4;
@@ -364,7 +459,7 @@ struct StreamLayout {
                 "bulk destinations and float4 rows 16-byte aligned");
 };
 
-template <int DK, int DV>
+template <int DK, int DV, bool kTree>
 __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const VerifyParams p) {
   using L = StreamLayout<DK>;
   extern __shared__ __align__(128) float sm[];
@@ -387,11 +482,13 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   float* sV = sm + L::OFF_V + warp * kKMax * kRowsPerWarp;
   float* sU = sm + L::OFF_U + warp * kKMax * kRowsPerWarp;
 
+  TreeTable* tree = reinterpret_cast<TreeTable*>(sm + L::OFF_TREE);
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
+    if constexpr (kTree) build_tree(p, b, tree, false);
   }
-  __syncthreads();  // the barrier is initialised before any thread polls it
+  __syncthreads();  // the barrier (and the tree table) are ready before any thread uses them
   if (tid == 0) {
     mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES);
     // S0: the previous final state, or (rollback applied on read) the accepted intermediate or
@@ -414,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   if (lane >= 4 && lane < 4 + kRowsPerWarp) {
     const int i = warp * kRowsPerWarp + (lane - 4);
     float y[kKMax];
-    conv_channel(p, b, 2 * p.Hk * DK + h * DV + r0 + i, y);
+    conv_channel<kTree>(p, b, 2 * p.Hk * DK + h * DV + r0 + i, tree, y);
 #pragma unroll
     for (int t = 0; t < kKMax; ++t) sV[t * kRowsPerWarp + (lane - 4)] = y[t];
   }
@@ -527,6 +624,17 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   const size_t head_tile_off = (size_t(h) * DV + r0) * DK;  // offset of this tile inside one token's states
   float* inter = p.state_inter ? p.state_inter + size_t(b) * (K - 1) * inter_stride + head_tile_off + my_off : nullptr;
   for (int t = 0; t < K; ++t) {
+    if constexpr (kTree) {
+      // a node that does not continue the previous one starts from its parent's state: S0 (still
+      // in shared memory) or the parent's intermediate, which this same lane stored earlier
+      const int par = tree->parent[t];
+      if (t > 0 && par != t - 1) {
+#pragma unroll
+        for (int q = 0; q < F4; ++q)
+          s[q] = (par < 0) ? *reinterpret_cast<const float4*>(sS0 + (row0 + rowq[q]) * DK + 4 * c4)
+                           : *reinterpret_cast<const float4*>(inter + size_t(par) * inter_stride + size_t(rowq[q]) * DK);
+      }
+    }
     const float g = gG[t];
     const float4 kv = *reinterpret_cast<const float4*>(sKn + t * DK + 4 * c4);
     float* dst = (t == K - 1) ? p.state_out + tile_off + my_off : inter + size_t(t) * inter_stride;
@@ -548,10 +656,10 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   }
 }
 
-template <int DK, int DV>
+template <int DK, int DV, bool kTree>
 cudaError_t launch_t(const VerifyParams& p, cudaStream_t stream) {
-  auto k1 = gdn_qk_prologue_kernel<DK>;
-  auto k2 = gdn_state_stream_kernel<DK, DV>;
+  auto k1 = gdn_qk_prologue_kernel<DK, kTree>;
+  auto k2 = gdn_state_stream_kernel<DK, DV, kTree>;
   const size_t b1 = PrologueLayout<DK>::BYTES;
   const size_t b2 = StreamLayout<DK>::BYTES;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, int(b1));
@@ -577,10 +685,14 @@ cudaError_t launch_t(const VerifyParams& p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {
-  if (p.dk == 128 && p.dv == 128) return launch_t<128, 128>(p, stream);
-  if (p.dk == 128 && p.dv == 64) return launch_t<128, 64>(p, stream);
-  if (p.dk == 64 && p.dv == 128) return launch_t<64, 128>(p, stream);
-  if (p.dk == 64 && p.dv == 64) return launch_t<64, 64>(p, stream);
+  const bool tree = p.parent != nullptr;
+#define GDN_LAUNCH(DK_, DV_) \
+  if (p.dk == DK_ && p.dv == DV_) return tree ? launch_t<DK_, DV_, true>(p, stream) : launch_t<DK_, DV_, false>(p, stream);
+  GDN_LAUNCH(128, 128)
+  GDN_LAUNCH(128, 64)
+  GDN_LAUNCH(64, 128)
+  GDN_LAUNCH(64, 64)
+#undef GDN_LAUNCH
   return cudaErrorInvalidValue;
 }
 

@@ -95,6 +95,13 @@ class GdnLayerState:
                             self.conv_states[i], self.conv_states[o], self.conv_inter, self.states[i],
                             self.states[o], self.state_inter, self.out, self.workspace, stream)
 
+    def verify_tree(self, parent, stream=None) -> None:
+        """Verify the loaded window as a token tree (parent [B, K] int32 on the device)."""
+        i, o = (self.cur, 1 - self.cur) if self.keep_snapshot else (0, 0)
+        gdn.gdn_verify_tree(self.dims, parent, self.x, self.a, self.b, self.A_log, self.dt_bias, self.conv_w,
+                            self.conv_states[i], self.conv_states[o], self.conv_inter, self.states[i],
+                            self.states[o], self.state_inter, self.out, self.workspace, stream)
+
     def rollback(self, stream=None) -> None:
         if self.keep_snapshot:
             i, o = self.cur, 1 - self.cur

@@ -145,6 +145,20 @@ def make_layer(g: Gen, d: Dims, dist: Dists) -> Layer:
     return Layer(conv_w, A_log, dt_bias, conv_state, state)
 
 
+def make_tree(g: Gen, B: int, K: int, p_chain: float = 0.5) -> np.ndarray:
+    """Random token trees in topological order: parent[b][t] in -1..t-1 (int32 [B, K]).
+
+    With probability p_chain a node continues the previous node (a chain segment); otherwise
+    its parent is drawn uniformly from -1..t-1 (a branch)."""
+    parent = np.empty((B, K), np.int32)
+    for bi in range(B):
+        cont = g.uniform((K,)) < p_chain
+        pick = g.uniform((K,))
+        for t in range(K):
+            parent[bi, t] = t - 1 if (t == 0 or cont[t]) else int(np.floor(pick[t] * (t + 1))) - 1
+    return parent
+
+
 def make_round(g: Gen, d: Dims, dist: Dists) -> Round:
     x = f32_to_bf16_bits(g.normal((d.B, d.K, d.C), dist.x_std).astype(np.float32))
     a = f32_to_bf16_bits(g.normal((d.B, d.K, d.Hv), dist.a_std).astype(np.float32))

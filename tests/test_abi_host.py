@@ -151,6 +151,16 @@ def test_rollback_validation(lib):
     assert lib.gdn_rollback(ctypes.byref(dims), *args, None) == gdn.GDN_ERR_INVALID_ARG
 
 
+def test_tree_validation(lib):
+    dims = gdn.make_dims(**BASE)
+    ptrs = _ptrs(NV)
+    assert lib.gdn_verify_tree(ctypes.byref(dims), None, *ptrs, ctypes.c_uint64(1 << 40), None) == gdn.GDN_ERR_INVALID_ARG
+    assert lib.gdn_verify_tree(ctypes.byref(dims), ctypes.c_void_p(P - 2), *ptrs, ctypes.c_uint64(1 << 40),
+                               None) == gdn.GDN_ERR_INVALID_ARG
+    # parent overlapping an output
+    assert lib.gdn_verify_tree(ctypes.byref(dims), ptrs[12], *ptrs, ctypes.c_uint64(1 << 40), None) == gdn.GDN_ERR_ALIAS
+
+
 def test_conv_step_validation(lib):
     dims = gdn.make_dims(**BASE)
     pt = _ptrs(5)

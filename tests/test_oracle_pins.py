@@ -366,3 +366,67 @@ def test_verify_step_splits_channels_q_k_v():
     gam = np.cumprod(g, axis=1)                                  # [B,K,Hv]
     for t in range(d.K):
         np.testing.assert_allclose(res["states"][:, t], gam[:, t, :, None, None] * lay.state, rtol=1e-12)
+
+
+# ---------------------------------------------------------------- token trees
+
+def _tree_problem(seed, parent, Hk=2, Hv=4, dk=6, dv=5):
+    parent = np.asarray(parent)
+    B, K = parent.shape
+    d = Dims(B=B, K=K, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+    g = Gen(seed)
+    lay = make_layer(g, d, Dists())
+    rnd = make_round(g, d, Dists())
+    return d, lay, rnd
+
+
+def _tree(d, lay, rnd, parent, **kw):
+    return O.tree_verify_step(d, parent, bf16_bits_to_f32(rnd.x), bf16_bits_to_f32(rnd.a), bf16_bits_to_f32(rnd.b),
+                              lay.A_log, lay.dt_bias, lay.conv_w, lay.conv_state, lay.state, **kw)
+
+
+def test_tree_of_a_chain_equals_the_window():
+    parent = np.array([[-1, 0, 1, 2, 3, 4], [-1, 0, 1, 2, 3, 4]])
+    d, lay, rnd = _tree_problem(40, parent)
+    tr = _tree(d, lay, rnd, parent, q_scale=0.8)
+    ch = _verify(d, lay, rnd, q_scale=0.8)
+    for key in ("out", "states", "conv_inter", "y"):
+        np.testing.assert_allclose(tr[key], ch[key], rtol=1e-13, atol=1e-14)
+
+
+def test_tree_nodes_equal_their_root_paths():
+    """Each node's output, state and history equal a plain window over its root-to-node path."""
+    parent = np.array([[-1, 0, 0, 1, -1, 3, 2, 6, 1], [-1, -1, 1, 0, 3, 3, 5, 2, 7]])
+    d, lay, rnd = _tree_problem(41, parent)
+    tr = _tree(d, lay, rnd, parent)
+    for bi in range(parent.shape[0]):
+        for t in range(parent.shape[1]):
+            path = O.tree_path(parent[bi], t)
+            dd = Dims(B=1, K=len(path), Hk=d.Hk, Hv=d.Hv, dk=d.dk, dv=d.dv)
+            sl = lambda z: z[bi:bi + 1][:, path]
+            ch = O.verify_step(dd, bf16_bits_to_f32(sl(rnd.x)), bf16_bits_to_f32(sl(rnd.a)), bf16_bits_to_f32(sl(rnd.b)),
+                               lay.A_log, lay.dt_bias, lay.conv_w, lay.conv_state[bi:bi + 1], lay.state[bi:bi + 1])
+            np.testing.assert_allclose(tr["out"][bi, t], ch["out"][0, -1], rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(tr["states"][bi, t], ch["state_out"][0], rtol=1e-12, atol=1e-13)
+            np.testing.assert_array_equal(tr["conv_inter"][bi, t], ch["conv_state_out"][0])
+
+
+def test_tree_star_is_independent_one_token_steps():
+    """All nodes children of the committed state: each is a one-token step from S0 (no
+    node sees another), so permuting the nodes permutes the results."""
+    parent = np.full((1, 5), -1)
+    d, lay, rnd = _tree_problem(42, parent)
+    tr = _tree(d, lay, rnd, parent)
+    perm = np.array([3, 0, 4, 1, 2])
+    from speculative_decode_verify_gdn_gb300.synth import Round
+    rp = Round(rnd.x[:, perm], rnd.a[:, perm], rnd.b[:, perm], rnd.accept_len)
+    tp = _tree(d, lay, rp, parent)
+    np.testing.assert_allclose(tp["out"], tr["out"][:, perm], rtol=1e-13)
+    np.testing.assert_allclose(tp["states"], tr["states"][:, perm], rtol=1e-13)
+
+
+def test_tree_rejects_bad_parents():
+    parent = np.array([[-1, 0, 2]])
+    d, lay, rnd = _tree_problem(43, parent)
+    with pytest.raises(ValueError):
+        _tree(d, lay, rnd, parent)
