@@ -287,3 +287,13 @@ def tree_path(parent_row, t):
         path.append(n)
         n = int(parent_row[n])
     return path[::-1]
+
+
+def gated_rms_norm(o, z, weight, eps: float = 1e-6):
+    """Output side of the GDN block: RMS norm of o over the v-head dim, times a learned weight
+    and the SiLU of the z gate (the attn_gate half of the stacked attn_gate|attn_qkv projection,
+    lucebox #637 commit list).  o, z [..., dv]; weight [dv]."""
+    o = np.asarray(o, np.float64)
+    z = np.asarray(z, np.float64)
+    w = np.asarray(weight, np.float64)
+    return o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps) * w * silu(z)

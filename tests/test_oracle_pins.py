@@ -430,3 +430,26 @@ def test_tree_rejects_bad_parents():
     d, lay, rnd = _tree_problem(43, parent)
     with pytest.raises(ValueError):
         _tree(d, lay, rnd, parent)
+
+
+# ---------------------------------------------------------------- gated output norm
+
+def test_gated_norm_hand_example():
+    gd = _read_named(os.path.join(GOLDEN, "gated_norm_hand.txt"))
+    out = O.gated_rms_norm(gd["o"], gd["z"], gd["w"], eps=gd["eps"][0])
+    np.testing.assert_allclose(out, gd["out"], rtol=1e-15, atol=1e-15)
+
+
+def test_gated_norm_scale_invariance_and_unit_rms():
+    rng = np.random.default_rng(7)
+    o = rng.standard_normal((3, 5, 128))
+    z = rng.standard_normal((3, 5, 128))
+    w = rng.uniform(0.5, 1.5, 128)
+    a = O.gated_rms_norm(o, z, w, eps=0.0)
+    np.testing.assert_allclose(O.gated_rms_norm(7.5 * o, z, w, eps=0.0), a, rtol=1e-13)
+    # dividing out weight and gate leaves a vector of unit RMS
+    core = a / (w * (z / (1 + np.exp(-z))))
+    np.testing.assert_allclose(np.sqrt(np.mean(core ** 2, axis=-1)), 1.0, rtol=1e-12)
+    # the gate enters through SiLU only: z -> large makes the gate the identity on z
+    big = O.gated_rms_norm(o, np.full_like(z, 40.0), np.ones(128), eps=0.0)
+    np.testing.assert_allclose(big, 40.0 * o / np.sqrt(np.mean(o ** 2, axis=-1, keepdims=True)), rtol=1e-13)
