@@ -200,7 +200,8 @@ def run_gdn(args):
     from speculative_decode_verify_gdn_gb300 import gdn
     from speculative_decode_verify_gdn_gb300.build import build_library, kernel_source_digest
     from speculative_decode_verify_gdn_gb300.runtime import GdnLayerState
-    from speculative_decode_verify_gdn_gb300.synth import WORKLOADS, Gen, make_layer, make_round, make_tree
+    from speculative_decode_verify_gdn_gb300.synth import (WORKLOADS, Gen, make_layer, make_output_gate, make_round,
+                                                            make_tree)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -319,6 +320,35 @@ def run_gdn(args):
     if gdn.gdn_device_status(clear=True):
         raise RuntimeError("device status flags after the tree steps")
 
+    # verify with the gated RMS output norm fused into the epilogue (gdn_verify_gated): z gate
+    # [B, K, Hv, dv] bf16 and the norm weight [dv] resident like the other inputs
+    zb, nw = make_output_gate(Gen(w.seed + 88), d)
+    zg = torch.from_numpy(zb.view(np.int16)).to(dev).view(torch.bfloat16)
+    nwg = torch.from_numpy(nw).to(dev)
+
+    def gated_step(i):
+        j = i % n_in
+        gdn.gdn_verify_gated(dims, xs[j], as_[j], bs[j], st.A_log, st.dt_bias, st.conv_w, CS, CS, CI, S0, S0, SI,
+                             zg, nwg, 1e-6, OUT, WS, stream)
+
+    for i in range(args.warmup):
+        gated_step(i)
+    barrier()
+    r0.record(stream)
+    n_gated = max(3, args.steps // 5)
+    for i in range(n_gated):
+        gated_step(i)
+    r1.record(stream)
+    barrier()
+    gms = max_over_ranks(r0.elapsed_time(r1), world, dev)
+    gbytes = verify_bytes(d, out_bytes=2) + zg.numel() * 2 + nwg.numel() * 4
+    gated = {"value": job_throughput(d.B * d.K * n_gated, world, gms), "unit": UNIT,
+             "ms_per_step": gms / n_gated, "steps": n_gated, "gpu_launches": 2 * n_gated,
+             "hbm_frac": gbytes / (gms / n_gated * 1e-3) / 1e9 / measured_peak_gbs()[0],
+             "what": "gdn_verify_gated per step: verify with the gated RMS output norm fused (no rollback)"}
+    if gdn.gdn_device_status(clear=True):
+        raise RuntimeError("device status flags after the gated steps")
+
     # e2e: inputs from pinned host memory and the output back, inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -381,6 +411,7 @@ def run_gdn(args):
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "zero_copy_rollback": resume,
         "tree_verify": tree,
+        "gated_verify": gated,
     }
     if world > 1:
         dist.barrier()

@@ -176,6 +176,29 @@ gdn_status gdn_verify_tree(const gdn_dims* dims, const int32_t* parent_dev, cons
                            void* workspace, uint64_t workspace_bytes, gdn_stream_t stream);
 
 /*
+ * gdn_verify_step with the output side of the GDN block fused into its
+ * epilogue: the gated RMS norm of each token's v-head output, with the z gate
+ * taken from the attn_gate half of the stacked attn_gate|attn_qkv projection
+ * (lucebox #637, "NVLink fix for PR625", commit list).  Per (b, t, h):
+ *   out[b,t,h,:] = o * w * SiLU(z[b,t,h,:]) / sqrt(mean_i(o_i^2) + norm_eps)
+ * where o is the step's (scaled) attention output before any rounding.
+ *  z        [B, K, Hv, dv] bf16, device, read only (16-byte aligned, may not
+ *           overlap an output).
+ *  norm_w   [dv] f32, device, read only: the norm weight, shared by all heads.
+ *  norm_eps finite, >= 0.
+ * Everything else (the states and histories written, aliasing, workspace,
+ * errors) is as for gdn_verify_step; `out` holds the normed result only.
+ * The v-head's row tiles run as one thread-block cluster, sharing the sums of
+ * squares through distributed shared memory.
+ */
+gdn_status gdn_verify_gated(const gdn_dims* dims, const uint16_t* x, const uint16_t* a, const uint16_t* b,
+                            const float* A_log, const float* dt_bias, const float* conv_w,
+                            const float* conv_state_in, float* conv_state_out, float* conv_inter,
+                            const float* state_in, float* state_out, float* state_inter, const uint16_t* z,
+                            const float* norm_w, float norm_eps, void* out, void* workspace,
+                            uint64_t workspace_bytes, gdn_stream_t stream);
+
+/*
  * Bytes of workspace gdn_verify_step needs for `dims`:
  * 4 * (B*Hk*(32*dk + 16*dk) + B*Hv*596).  Validates dims like gdn_verify_step.
  */

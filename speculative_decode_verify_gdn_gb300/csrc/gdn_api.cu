@@ -105,6 +105,9 @@ struct VerifyArgs {
   bool resume;
   const int32_t* accept_prev;
   const int32_t* parent;  // token tree (gdn_verify_tree) or null
+  const uint16_t* z;      // gated output norm (gdn_verify_gated) or null
+  const float* norm_w;
+  float norm_eps;
   const uint16_t *x, *a, *b;
   const float *A_log, *dt_bias, *conv_w;
   const float* conv_state_in;
@@ -162,6 +165,11 @@ gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t s
   }
   if (v.parent && (reinterpret_cast<uintptr_t>(v.parent) & 3u))
     return fail(GDN_ERR_INVALID_ARG, "parent misaligned");
+  if (v.z) {
+    GDN_CHECK_PTR(v.norm_w, "norm_w");
+    if (!std::isfinite(v.norm_eps) || v.norm_eps < 0.f)
+      return fail(GDN_ERR_INVALID_ARG, "norm_eps must be finite, >= 0");
+  }
   const size_t ws_need = gdn::workspace_bytes(d.B, d.Hk, d.Hv, d.dk);
   if (v.workspace_bytes < ws_need)
     return fail(GDN_ERR_INVALID_ARG, "workspace has %llu bytes, needs %zu", (unsigned long long)v.workspace_bytes,
@@ -186,6 +194,8 @@ gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t s
       {"state_snapshot_prev", range_of(v.state_snap_prev, B * S * 4), false},
       {"accept_len_prev", range_of(v.accept_prev, B * 4), false},
       {"parent", range_of(v.parent, B * K * 4), false},
+      {"z", range_of(v.z, B * K * d.Hv * d.dv * 2), false},
+      {"norm_w", range_of(v.z ? v.norm_w : nullptr, size_t(d.dv) * 4), false},
       {"conv_state_out", range_of(v.conv_state_out, B * 3 * C * 4), true},
       {"conv_inter", range_of(v.conv_inter, B * K * 3 * C * 4), true},
       {"state_out", range_of(v.state_out, B * S * 4), true},
@@ -230,6 +240,9 @@ gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t s
   p.out = v.out;
   p.ws = gdn::workspace_carve(v.workspace, d.B, d.Hk, d.Hv, d.dk);
   p.parent = v.parent;
+  p.z = v.z;
+  p.norm_w = v.z ? v.norm_w : nullptr;
+  p.norm_eps = v.norm_eps;
   if (v.resume) {
     p.accept_prev = v.accept_prev;
     p.state_inter_prev = k1 ? nullptr : v.state_inter_prev;
@@ -346,6 +359,35 @@ gdn_status gdn_verify_tree(const gdn_dims* dims, const int32_t* parent_dev, cons
   if (dims && dims->B > 0 && !parent_dev) return fail(GDN_ERR_INVALID_ARG, "parent is NULL");
   VerifyArgs v{};
   v.parent = parent_dev;
+  v.x = x;
+  v.a = a;
+  v.b = b;
+  v.A_log = A_log;
+  v.dt_bias = dt_bias;
+  v.conv_w = conv_w;
+  v.conv_state_in = conv_state_in;
+  v.conv_state_out = conv_state_out;
+  v.conv_inter = conv_inter;
+  v.state_in = state_in;
+  v.state_out = state_out;
+  v.state_inter = state_inter;
+  v.out = out;
+  v.workspace = workspace;
+  v.workspace_bytes = workspace_bytes;
+  return verify_impl(dims, v, stream);
+}
+
+gdn_status gdn_verify_gated(const gdn_dims* dims, const uint16_t* x, const uint16_t* a, const uint16_t* b,
+                            const float* A_log, const float* dt_bias, const float* conv_w,
+                            const float* conv_state_in, float* conv_state_out, float* conv_inter,
+                            const float* state_in, float* state_out, float* state_inter, const uint16_t* z,
+                            const float* norm_w, float norm_eps, void* out, void* workspace,
+                            uint64_t workspace_bytes, gdn_stream_t stream) {
+  if (dims && dims->B > 0) GDN_CHECK_PTR(z, "z");
+  VerifyArgs v{};
+  v.z = z;
+  v.norm_w = norm_w;
+  v.norm_eps = norm_eps;
   v.x = x;
   v.a = a;
   v.b = b;

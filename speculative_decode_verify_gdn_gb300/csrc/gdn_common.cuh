@@ -1,8 +1,9 @@
 // Shared device helpers for the GDN verify library (sm_103a).
 //
 // Inline PTX for the Blackwell data-movement primitives the kernels use:
-// mbarrier transaction barriers and 1-D bulk async copies (cp.async.bulk, the
-// TMA engine's linear mode).  Nothing here touches the method's arithmetic.
+// mbarrier transaction barriers, 1-D bulk async copies (cp.async.bulk, the TMA
+// engine's linear mode), thread-block-cluster barriers and distributed shared
+// memory stores.  Nothing here touches the method's arithmetic.
 #pragma once
 
 #include <cstdint>
@@ -86,6 +87,36 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
           smem_addr(smem_dst)),
       "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
+}
+
+// ---------------------------------------------------------------- thread-block clusters
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Address of the same shared-memory variable in CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_smem_addr), "r"(rank));
+  return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- misc math helpers

@@ -61,6 +61,10 @@ struct VerifyParams {
   const float* conv_snap_prev;
   // Token tree (gdn_verify_tree; null for a chain window): parent[b][t] in -1..t-1.
   const int32_t* parent;
+  // Gated output norm (gdn_verify_gated; z null otherwise): out = o rsqrt(mean o^2 + eps) w SiLU(z)
+  const uint16_t* z;     // [B, K, Hv, dv] bf16
+  const float* norm_w;   // [dv]
+  float norm_eps;
   uint32_t* err;       // device status word
   int B, K, Hk, Hv, dk, dv, C;
   float q_scale, l2_eps;

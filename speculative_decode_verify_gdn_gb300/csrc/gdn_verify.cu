@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
 
 // ------------------------------------------------------------------------------------------
 // Kernel 2: per (sequence, v-head, 32-row tile) state stream.
-template <int DK>
+template <int DK, bool kGated = false>
 struct StreamLayout {
   static constexpr int PSTRIDE = kNCol + 4;                    // 16-byte rows
   static constexpr int RSTRIDE = kKMax + 1;
@@ -445,23 +445,31 @@ struct StreamLayout {
   static constexpr int OFF_V = OFF_KN + kKMax * DK;              // [warp][16][4] v conv outputs
   static constexpr int OFF_U = OFF_V + kWarps * kKMax * kRowsPerWarp;  // [warp][16][4] u
   static constexpr int OFF_P = OFF_U + kWarps * kKMax * kRowsPerWarp;  // [32][PSTRIDE] S0 [k^ | q^]
-  static constexpr int OFF_R = OFF_P + kRows * PSTRIDE;                // [32][RSTRIDE] rhs
-  static constexpr int OFF_TREE = OFF_R + kRows * RSTRIDE;              // TreeTable (token trees only)
-  static constexpr int OFF_BAR = (OFF_TREE + int(sizeof(TreeTable) / 4) + 1) & ~1;  // 8-byte aligned mbarrier
+  static constexpr int OFF_R = OFF_P + kRows * PSTRIDE;                // [32][RSTRIDE] rhs, then o (gated)
+  static constexpr int OFF_X = OFF_R + kRows * RSTRIDE;                // tree table or gated-norm block
+  static constexpr int OFF_TREE = OFF_X;                                 // TreeTable (token trees only)
+  static constexpr int OFF_SQ = OFF_X;                                   // gated: per-tile sums of o^2 [4][16]
+  static constexpr int OFF_NW = OFF_SQ + 4 * kKMax;                      // gated: norm weight [32], bulk copy
+  static constexpr int OFF_Z = OFF_NW + kRows;                           // gated: z [16][32] bf16, bulk copies
+  static constexpr int X_FLOATS = kGated ? 4 * kKMax + kRows + kKMax * kRows / 2 : int(sizeof(TreeTable) / 4);
+  static constexpr int OFF_BAR = (OFF_X + X_FLOATS + 1) & ~1;            // 8-byte aligned mbarrier
   static constexpr int FLOATS = OFF_BAR + 2;
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
   static constexpr uint32_t S0_BYTES = kRows * DK * 4;
   static constexpr uint32_t WT_BYTES = DK * kNCol * 4;
   static constexpr uint32_t GATE_BYTES = kGateFloats * 4;
   static constexpr uint32_t KN_BYTES = kKMax * DK * 4;
+  static constexpr uint32_t kRowsBytesW = kRows * 4;
+  static_assert(OFF_NW % 4 == 0 && OFF_Z % 4 == 0, "gated-norm bulk destinations 16-byte aligned");
   static_assert(S0_BYTES % 16 == 0 && WT_BYTES % 16 == 0 && GATE_BYTES % 16 == 0 && KN_BYTES % 16 == 0, "");
   static_assert(OFF_WT % 4 == 0 && OFF_GATE % 4 == 0 && OFF_KN % 4 == 0 && OFF_P % 4 == 0,
                 "bulk destinations and float4 rows 16-byte aligned");
 };
 
-template <int DK, int DV, bool kTree>
+template <int DK, int DV, bool kTree, bool kGated>
 __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const VerifyParams p) {
-  using L = StreamLayout<DK>;
+  static_assert(!(kTree && kGated), "tree and gated-norm variants are separate");
+  using L = StreamLayout<DK, kGated>;
   extern __shared__ __align__(128) float sm[];
   float* sS0 = sm + L::OFF_S0;
   float* sWT = sm + L::OFF_WT;
@@ -488,9 +496,18 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
     fence_mbar_init();
     if constexpr (kTree) build_tree(p, b, tree, false);
   }
+  if constexpr (kGated) cluster_arrive_relaxed();  // this CTA runs: the head's peers may write its smem later
   __syncthreads();  // the barrier (and the tree table) are ready before any thread uses them
   if (tid == 0) {
-    mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES);
+    uint32_t extra = 0;
+    if constexpr (kGated) extra = L::kRowsBytesW + uint32_t(K) * kRows * 2;
+    mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES + extra);
+    if constexpr (kGated) {
+      bulk_load(sm + L::OFF_NW, p.norm_w + r0, L::kRowsBytesW, bar);
+      for (int t = 0; t < K; ++t)
+        bulk_load(reinterpret_cast<uint16_t*>(sm + L::OFF_Z) + t * kRows,
+                  p.z + ((size_t(b) * K + t) * p.Hv + h) * DV + r0, kRows * 2, bar);
+    }
     // S0: the previous final state, or (rollback applied on read) the accepted intermediate or
     // the pre-window snapshot of the previous window
     const int Lp = prev_accept(p, b, blockIdx.x == 0);
@@ -525,8 +542,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (!ok) {
     if (lane == 0) atomicOr(p.err, kDevErrTimeout);
-    return;
+    if constexpr (!kGated) return;
   }
+  if (ok) {  // (a gated CTA's warps reach the cluster barriers at the end even after a timeout)
   (void)mbar_try_wait(bar, 0);  // every lane observes the completed phase
 
   const float* gM = sGate;
@@ -595,11 +613,15 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
     if (t < K) {
       float o = p.q_scale * gGam[t] * sP[(row0 + m) * L::PSTRIDE + kKMax + t];
       for (int jj = 0; jj <= t; ++jj) o = fmaf(gN[t * kMStride + jj], sU[jj * kRowsPerWarp + m], o);
-      const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
-      if (p.out_f32)
-        static_cast<float*>(p.out)[oi] = o;
-      else
-        static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(o);
+      if constexpr (kGated) {
+        sR[(row0 + m) * L::RSTRIDE + t] = o;  // the rhs rows of this warp are dead after the substitution
+      } else {
+        const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
+        if (p.out_f32)
+          static_cast<float*>(p.out)[oi] = o;
+        else
+          static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(o);
+      }
     }
   }
   __syncwarp();
@@ -654,14 +676,47 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
         __stcs(d4, s[q]);
     }
   }
+  }  // ok
+
+  if constexpr (kGated) {
+    // gated output norm over the head's dv rows, which the cluster's kTiles CTAs share: per
+    // token, this tile's sum of o^2 goes to every CTA of the cluster, then each CTA finishes its
+    // own rows: out = o rsqrt(sum / dv + eps) w SiLU(z)
+    __syncthreads();  // every warp's o is in shared memory
+    const uint32_t rank = cluster_ctarank();
+    const float* sO = sm + L::OFF_R;  // o of token t, row i at [i][t]
+    float* sSq = sm + L::OFF_SQ;
+    float part = 0.f;
+    if (tid < K)
+      for (int i = 0; i < kRows; ++i) part = fmaf(sO[i * L::RSTRIDE + tid], sO[i * L::RSTRIDE + tid], part);
+    cluster_wait_acquire();  // every CTA of the cluster has started (pairs with the arrive above)
+    if (tid < K)
+      for (int d = 0; d < kTiles; ++d) st_cluster_f32(map_to_rank(smem_addr(sSq + rank * kKMax + tid), d), part);
+    cluster_arrive_release();
+    cluster_wait_acquire();  // all sums are here; no shared memory of a peer is touched after this
+    const uint16_t* sZ = reinterpret_cast<const uint16_t*>(sm + L::OFF_Z);
+    for (int idx = tid; idx < K * kRows; idx += kThreads) {
+      const int t = idx / kRows, i = idx % kRows;
+      float tot = 0.f;
+#pragma unroll
+      for (int d = 0; d < kTiles; ++d) tot += sSq[d * kKMax + t];
+      const float inv = rsqrtf(tot * (1.f / DV) + p.norm_eps);
+      const float y = sO[i * L::RSTRIDE + t] * inv * sm[L::OFF_NW + i] * silu(bf16_to_f32(sZ[t * kRows + i]));
+      const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + i;
+      if (p.out_f32)
+        static_cast<float*>(p.out)[oi] = y;
+      else
+        static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(y);
+    }
+  }
 }
 
-template <int DK, int DV, bool kTree>
+template <int DK, int DV, bool kTree, bool kGated>
 cudaError_t launch_t(const VerifyParams& p, cudaStream_t stream) {
   auto k1 = gdn_qk_prologue_kernel<DK, kTree>;
-  auto k2 = gdn_state_stream_kernel<DK, DV, kTree>;
+  auto k2 = gdn_state_stream_kernel<DK, DV, kTree, kGated>;
   const size_t b1 = PrologueLayout<DK>::BYTES;
-  const size_t b2 = StreamLayout<DK>::BYTES;
+  const size_t b2 = StreamLayout<DK, kGated>::BYTES;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, int(b1));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, int(b2));
@@ -674,11 +729,18 @@ cudaError_t launch_t(const VerifyParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = b2;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if constexpr (kGated) {  // the row tiles of one v-head form a cluster (they share the output norm)
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = DV / kRows;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, k2, p);
 }
 
@@ -686,8 +748,13 @@ cudaError_t launch_t(const VerifyParams& p, cudaStream_t stream) {
 
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {
   const bool tree = p.parent != nullptr;
-#define GDN_LAUNCH(DK_, DV_) \
-  if (p.dk == DK_ && p.dv == DV_) return tree ? launch_t<DK_, DV_, true>(p, stream) : launch_t<DK_, DV_, false>(p, stream);
+  const bool gated = p.z != nullptr;
+#define GDN_LAUNCH(DK_, DV_)                                          \
+  if (p.dk == DK_ && p.dv == DV_) {                                   \
+    if (gated) return launch_t<DK_, DV_, false, true>(p, stream);     \
+    if (tree) return launch_t<DK_, DV_, true, false>(p, stream);      \
+    return launch_t<DK_, DV_, false, false>(p, stream);               \
+  }
   GDN_LAUNCH(128, 128)
   GDN_LAUNCH(128, 64)
   GDN_LAUNCH(64, 128)

@@ -14,8 +14,9 @@ import torch
 
 from .build import LIB_PATH
 
-EXPORTED = ("gdn_conv_step", "gdn_verify_step", "gdn_verify_resume", "gdn_verify_tree", "gdn_verify_workspace_size",
-            "gdn_verify_step_static_scratch", "gdn_rollback", "gdn_device_status", "gdn_last_error")
+EXPORTED = ("gdn_conv_step", "gdn_verify_step", "gdn_verify_resume", "gdn_verify_tree", "gdn_verify_gated",
+            "gdn_verify_workspace_size", "gdn_verify_step_static_scratch", "gdn_rollback", "gdn_device_status",
+            "gdn_last_error")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIAS, GDN_ERR_NO_SNAPSHOT, GDN_ERR_CUDA = range(6)
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIAS",
@@ -61,14 +62,15 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdn_verify_step.argtypes = [D] + [P] * 14 + [ctypes.c_uint64, P]
     lib.gdn_verify_resume.argtypes = [D] + [P] * 19 + [ctypes.c_uint64, P]
     lib.gdn_verify_tree.argtypes = [D] + [P] * 15 + [ctypes.c_uint64, P]
+    lib.gdn_verify_gated.argtypes = [D] + [P] * 14 + [ctypes.c_float, P, P, ctypes.c_uint64, P]
     lib.gdn_verify_workspace_size.argtypes = [D, ctypes.POINTER(ctypes.c_uint64)]
     lib.gdn_verify_step_static_scratch.argtypes = [D] + [P] * 14
     lib.gdn_rollback.argtypes = [D] + [P] * 8
     lib.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32, P]
     lib.gdn_last_error.argtypes = []
     lib.gdn_last_error.restype = ctypes.c_char_p
-    for f in ("gdn_conv_step", "gdn_verify_step", "gdn_verify_resume", "gdn_verify_tree", "gdn_verify_workspace_size",
-              "gdn_verify_step_static_scratch", "gdn_rollback", "gdn_device_status"):
+    for f in ("gdn_conv_step", "gdn_verify_step", "gdn_verify_resume", "gdn_verify_tree", "gdn_verify_gated",
+              "gdn_verify_workspace_size", "gdn_verify_step_static_scratch", "gdn_rollback", "gdn_device_status"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -169,6 +171,27 @@ def gdn_verify_tree(dims: GdnDims, parent, x, a, b, A_log, dt_bias, conv_w, conv
         _ptr(state_inter, "state_inter", torch.float32, d.B * (d.K - 1) * S, allow_none=(d.K == 1)),
         _ptr(out, "out", odt, BK * d.Hv * d.dv), _ws_ptr(workspace), ctypes.c_uint64(_ws_bytes(workspace)),
         _stream(stream)))
+
+
+def gdn_verify_gated(dims: GdnDims, x, a, b, A_log, dt_bias, conv_w, conv_state_in, conv_state_out, conv_inter,
+                     state_in, state_out, state_inter, z, norm_w, norm_eps, out, workspace, stream=None) -> None:
+    """a1..a4 with the gated RMS norm fused into the output: z [B, K, Hv, dv] bf16, norm_w [dv] f32."""
+    d = dims
+    C, BK = d.C, d.B * d.K
+    S = d.Hv * d.dv * d.dk
+    odt = torch.float32 if d.out_f32 else torch.bfloat16
+    _check(load_library().gdn_verify_gated(
+        ctypes.byref(d), _ptr(x, "x", torch.bfloat16, BK * C), _ptr(a, "a", torch.bfloat16, BK * d.Hv),
+        _ptr(b, "b", torch.bfloat16, BK * d.Hv), _ptr(A_log, "A_log", torch.float32, d.Hv),
+        _ptr(dt_bias, "dt_bias", torch.float32, d.Hv), _ptr(conv_w, "conv_w", torch.float32, C * d.conv_w),
+        _ptr(conv_state_in, "conv_state_in", torch.float32, d.B * (d.conv_w - 1) * C),
+        _ptr(conv_state_out, "conv_state_out", torch.float32, d.B * (d.conv_w - 1) * C),
+        _ptr(conv_inter, "conv_inter", torch.float32, BK * (d.conv_w - 1) * C, allow_none=True),
+        _ptr(state_in, "state_in", torch.float32, d.B * S), _ptr(state_out, "state_out", torch.float32, d.B * S),
+        _ptr(state_inter, "state_inter", torch.float32, d.B * (d.K - 1) * S, allow_none=(d.K == 1)),
+        _ptr(z, "z", torch.bfloat16, BK * d.Hv * d.dv), _ptr(norm_w, "norm_w", torch.float32, d.dv),
+        ctypes.c_float(norm_eps), _ptr(out, "out", odt, BK * d.Hv * d.dv), _ws_ptr(workspace),
+        ctypes.c_uint64(_ws_bytes(workspace)), _stream(stream)))
 
 
 def gdn_verify_resume(dims: GdnDims, accept_len_prev, x, a, b, A_log, dt_bias, conv_w, conv_state_in,

@@ -102,6 +102,15 @@ class GdnLayerState:
                             self.conv_states[i], self.conv_states[o], self.conv_inter, self.states[i],
                             self.states[o], self.state_inter, self.out, self.workspace, stream)
 
+    def verify_gated(self, z, norm_w, norm_eps=1e-6, stream=None) -> None:
+        """Verify the loaded window with the gated RMS norm fused into the output
+        (z [B, K, Hv, dv] bf16 and norm_w [dv] f32 on the device)."""
+        i, o = (self.cur, 1 - self.cur) if self.keep_snapshot else (0, 0)
+        gdn.gdn_verify_gated(self.dims, self.x, self.a, self.b, self.A_log, self.dt_bias, self.conv_w,
+                             self.conv_states[i], self.conv_states[o], self.conv_inter, self.states[i],
+                             self.states[o], self.state_inter, z, norm_w, norm_eps, self.out, self.workspace,
+                             stream)
+
     def rollback(self, stream=None) -> None:
         if self.keep_snapshot:
             i, o = self.cur, 1 - self.cur

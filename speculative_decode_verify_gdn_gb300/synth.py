@@ -159,6 +159,14 @@ def make_tree(g: Gen, B: int, K: int, p_chain: float = 0.5) -> np.ndarray:
     return parent
 
 
+def make_output_gate(g: Gen, d: Dims, z_std: float = 1.0, w_std: float = 0.1):
+    """Inputs of the gated output norm: z [B, K, Hv, dv] as bf16 bits and the norm weight
+    [dv] f32 drawn around 1."""
+    z = f32_to_bf16_bits(g.normal((d.B, d.K, d.Hv, d.dv), z_std).astype(np.float32))
+    w = (1.0 + g.normal((d.dv,), w_std)).astype(np.float32)
+    return z, w
+
+
 def make_round(g: Gen, d: Dims, dist: Dists) -> Round:
     x = f32_to_bf16_bits(g.normal((d.B, d.K, d.C), dist.x_std).astype(np.float32))
     a = f32_to_bf16_bits(g.normal((d.B, d.K, d.Hv), dist.a_std).astype(np.float32))

@@ -161,6 +161,25 @@ def test_tree_validation(lib):
     assert lib.gdn_verify_tree(ctypes.byref(dims), ptrs[12], *ptrs, ctypes.c_uint64(1 << 40), None) == gdn.GDN_ERR_ALIAS
 
 
+def test_gated_validation(lib):
+    dims = gdn.make_dims(**BASE)
+
+    def call(z_null=False, w_null=False, eps=1e-6, z=None):
+        pt = _ptrs(16)
+        zp = None if z_null else (z if z is not None else pt[12])
+        wp = None if w_null else pt[13]
+        return lib.gdn_verify_gated(ctypes.byref(dims), *pt[:12], zp, wp, ctypes.c_float(eps), pt[14], pt[15],
+                                    ctypes.c_uint64(1 << 40), None)
+
+    assert call(z_null=True) == gdn.GDN_ERR_INVALID_ARG and "z" in gdn.last_error()
+    assert call(w_null=True) == gdn.GDN_ERR_INVALID_ARG and "norm_w" in gdn.last_error()
+    assert call(eps=float("nan")) == gdn.GDN_ERR_INVALID_ARG
+    assert call(eps=-1.0) == gdn.GDN_ERR_INVALID_ARG
+    assert call(z=ctypes.c_void_p(P + 12 * MB + 8)) == gdn.GDN_ERR_INVALID_ARG   # misaligned
+    assert call(z=ctypes.c_void_p(P + 14 * MB)) == gdn.GDN_ERR_ALIAS            # z overlapping out
+    assert "z" in gdn.last_error()
+
+
 def test_conv_step_validation(lib):
     dims = gdn.make_dims(**BASE)
     pt = _ptrs(5)
