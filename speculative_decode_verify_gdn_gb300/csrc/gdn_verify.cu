@@ -448,10 +448,9 @@ struct StreamLayout {
   static constexpr int OFF_R = OFF_P + kRows * PSTRIDE;                // [32][RSTRIDE] rhs, then o (gated)
   static constexpr int OFF_X = OFF_R + kRows * RSTRIDE;                // tree table or gated-norm block
   static constexpr int OFF_TREE = OFF_X;                                 // TreeTable (token trees only)
-  static constexpr int OFF_SQ = OFF_X;                                   // gated: per-tile sums of o^2 [4][16]
-  static constexpr int OFF_NW = OFF_SQ + 4 * kKMax;                      // gated: norm weight [32], bulk copy
-  static constexpr int OFF_Z = OFF_NW + kRows;                           // gated: z [16][32] bf16, bulk copies
-  static constexpr int X_FLOATS = kGated ? 4 * kKMax + kRows + kKMax * kRows / 2 : int(sizeof(TreeTable) / 4);
+  static constexpr int OFF_SQ = OFF_X;                                   // gated: sums of o^2 [tile][warp][16]
+  static constexpr int OFF_NW = OFF_SQ + 4 * kWarps * kKMax;             // gated: norm weight [32], bulk copy
+  static constexpr int X_FLOATS = kGated ? 4 * kWarps * kKMax + kRows : int(sizeof(TreeTable) / 4);
   static constexpr int OFF_BAR = (OFF_X + X_FLOATS + 1) & ~1;            // 8-byte aligned mbarrier
   static constexpr int FLOATS = OFF_BAR + 2;
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
@@ -460,7 +459,7 @@ struct StreamLayout {
   static constexpr uint32_t GATE_BYTES = kGateFloats * 4;
   static constexpr uint32_t KN_BYTES = kKMax * DK * 4;
   static constexpr uint32_t kRowsBytesW = kRows * 4;
-  static_assert(OFF_NW % 4 == 0 && OFF_Z % 4 == 0, "gated-norm bulk destinations 16-byte aligned");
+  static_assert(OFF_NW % 4 == 0, "gated-norm bulk destination 16-byte aligned");
   static_assert(S0_BYTES % 16 == 0 && WT_BYTES % 16 == 0 && GATE_BYTES % 16 == 0 && KN_BYTES % 16 == 0, "");
   static_assert(OFF_WT % 4 == 0 && OFF_GATE % 4 == 0 && OFF_KN % 4 == 0 && OFF_P % 4 == 0,
                 "bulk destinations and float4 rows 16-byte aligned");
@@ -498,16 +497,20 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   }
   if constexpr (kGated) cluster_arrive_relaxed();  // this CTA runs: the head's peers may write its smem later
   __syncthreads();  // the barrier (and the tree table) are ready before any thread uses them
+  // gated: this thread's two z values of the epilogue, (token tid/32, row tid%32) and eight
+  // tokens later, fetched now so that they have long arrived when the epilogue runs
+  uint32_t zz = 0;
+  if constexpr (kGated) {
+    const int t0 = tid / kRows, i0 = tid % kRows;
+    const uint16_t* zp = p.z + ((size_t(b) * K + t0) * p.Hv + h) * DV + r0 + i0;
+    if (t0 < K) zz = __ldg(zp);
+    if (t0 + 8 < K) zz |= uint32_t(__ldg(zp + size_t(8) * p.Hv * DV)) << 16;
+  }
   if (tid == 0) {
     uint32_t extra = 0;
-    if constexpr (kGated) extra = L::kRowsBytesW + uint32_t(K) * kRows * 2;
+    if constexpr (kGated) extra = L::kRowsBytesW;
     mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES + extra);
-    if constexpr (kGated) {
-      bulk_load(sm + L::OFF_NW, p.norm_w + r0, L::kRowsBytesW, bar);
-      for (int t = 0; t < K; ++t)
-        bulk_load(reinterpret_cast<uint16_t*>(sm + L::OFF_Z) + t * kRows,
-                  p.z + ((size_t(b) * K + t) * p.Hv + h) * DV + r0, kRows * 2, bar);
-    }
+    if constexpr (kGated) bulk_load(sm + L::OFF_NW, p.norm_w + r0, L::kRowsBytesW, bar);
     // S0: the previous final state, or (rollback applied on read) the accepted intermediate or
     // the pre-window snapshot of the previous window
     const int Lp = prev_accept(p, b, blockIdx.x == 0);
@@ -541,12 +544,13 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   if (lane == 0) ok = mbar_wait_bounded(bar, 0) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   if (!ok) {
-    if (lane == 0) atomicOr(p.err, kDevErrTimeout);
+    if (lane == 0) {
+      atomicOr(p.err, kDevErrTimeout);
+      (void)mbar_wait_bounded(bar, 0);  // give the copies in flight one more bounded wait
+    }
+    __syncwarp();
     if constexpr (!kGated) return;
   }
-  if (ok) {  // (a gated CTA's warps reach the cluster barriers at the end even after a timeout)
-  (void)mbar_try_wait(bar, 0);  // every lane observes the completed phase
-
   const float* gM = sGate;
   const float* gN = sGate + kGateOffN;
   const float* gBeta = sGate + kGateOffBeta;
@@ -557,6 +561,11 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   const int row0 = warp * kRowsPerWarp;
   const int m = lane >> 3;   // row of this warp handled by this lane in the phases below
   const int cg = lane & 7;   // column group (P) / token (outputs)
+
+  // (a gated CTA's warps take part in the cluster barriers below even after a timeout)
+  float sq_a = 0.f, sq_b = 0.f;  // gated: o^2 of tokens cg and cg + 8, summed over the warp's rows
+  if (ok) {
+  (void)mbar_try_wait(bar, 0);  // every lane observes the completed phase
 
   // P = S0 [k^ | q^]: lane (m, cg) computes columns 4cg..4cg+3 of row row0+m; for the k^
   // columns the right-hand side rhs_j = v_j - Gamma_j (S0 k^_j) right away
@@ -615,6 +624,10 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
       for (int jj = 0; jj <= t; ++jj) o = fmaf(gN[t * kMStride + jj], sU[jj * kRowsPerWarp + m], o);
       if constexpr (kGated) {
         sR[(row0 + m) * L::RSTRIDE + t] = o;  // the rhs rows of this warp are dead after the substitution
+        if (half == 0)
+          sq_a = o * o;
+        else
+          sq_b = o * o;
       } else {
         const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
         if (p.out_f32)
@@ -625,7 +638,29 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
     }
   }
   __syncwarp();
+  }  // ok
 
+  const uint32_t rank = kGated ? cluster_ctarank() : 0;
+  if constexpr (kGated) {
+    // sums of o^2 over the warp's 4 rows (lanes m = 0..3 of one column group), sent to every CTA
+    // of the cluster; nobody waits for them until the epilogue
+    sq_a += __shfl_xor_sync(0xffffffffu, sq_a, 8);
+    sq_a += __shfl_xor_sync(0xffffffffu, sq_a, 16);
+    sq_b += __shfl_xor_sync(0xffffffffu, sq_b, 8);
+    sq_b += __shfl_xor_sync(0xffffffffu, sq_b, 16);
+    cluster_wait_acquire();  // every CTA of the cluster has started (pairs with the first arrive)
+    if (lane < 8) {
+      const uint32_t slot = smem_addr(sm + L::OFF_SQ + (rank * kWarps + warp) * kKMax + lane);
+      for (int d = 0; d < kTiles; ++d) {
+        const uint32_t a = map_to_rank(slot, d);
+        st_cluster_f32(a, sq_a);
+        st_cluster_f32(a + 8 * 4, sq_b);
+      }
+    }
+    cluster_arrive_release();
+  }
+
+  if (ok) {
   // stream the K states from registers: lane owns DK/32 float4 of the warp's 4 rows
   constexpr int F4 = DK / 32;
   constexpr int C4 = DK / 4;
@@ -679,34 +714,29 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   }  // ok
 
   if constexpr (kGated) {
-    // gated output norm over the head's dv rows, which the cluster's kTiles CTAs share: per
-    // token, this tile's sum of o^2 goes to every CTA of the cluster, then each CTA finishes its
-    // own rows: out = o rsqrt(sum / dv + eps) w SiLU(z)
-    __syncthreads();  // every warp's o is in shared memory
-    const uint32_t rank = cluster_ctarank();
+    // gated output norm over the head's dv rows, which the cluster's kTiles CTAs share:
+    // out = o rsqrt(sum_rows o^2 / dv + eps) w SiLU(z).  The wait pairs with every peer's arrive
+    // after its outputs phase, long past; it also orders this CTA's own o rows (written before its
+    // arrive) before the reads below, and no peer writes to this CTA's shared memory after it.
+    (void)rank;
+    cluster_wait_acquire();
     const float* sO = sm + L::OFF_R;  // o of token t, row i at [i][t]
-    float* sSq = sm + L::OFF_SQ;
-    float part = 0.f;
-    if (tid < K)
-      for (int i = 0; i < kRows; ++i) part = fmaf(sO[i * L::RSTRIDE + tid], sO[i * L::RSTRIDE + tid], part);
-    cluster_wait_acquire();  // every CTA of the cluster has started (pairs with the arrive above)
-    if (tid < K)
-      for (int d = 0; d < kTiles; ++d) st_cluster_f32(map_to_rank(smem_addr(sSq + rank * kKMax + tid), d), part);
-    cluster_arrive_release();
-    cluster_wait_acquire();  // all sums are here; no shared memory of a peer is touched after this
-    const uint16_t* sZ = reinterpret_cast<const uint16_t*>(sm + L::OFF_Z);
-    for (int idx = tid; idx < K * kRows; idx += kThreads) {
-      const int t = idx / kRows, i = idx % kRows;
-      float tot = 0.f;
+    const float* sSq = sm + L::OFF_SQ;
 #pragma unroll
-      for (int d = 0; d < kTiles; ++d) tot += sSq[d * kKMax + t];
-      const float inv = rsqrtf(tot * (1.f / DV) + p.norm_eps);
-      const float y = sO[i * L::RSTRIDE + t] * inv * sm[L::OFF_NW + i] * silu(bf16_to_f32(sZ[t * kRows + i]));
-      const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + i;
-      if (p.out_f32)
-        static_cast<float*>(p.out)[oi] = y;
-      else
-        static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(y);
+    for (int half = 0; half < 2; ++half) {
+      const int t = tid / kRows + 8 * half, i = tid % kRows;
+      if (t < K) {
+        float tot = 0.f;
+        for (int d = 0; d < kTiles * kWarps; ++d) tot += sSq[d * kKMax + t];
+        const float inv = rsqrtf(tot * (1.f / DV) + p.norm_eps);
+        const float zf = bf16_to_f32(uint16_t(half ? zz >> 16 : zz & 0xFFFFu));
+        const float y = sO[i * L::RSTRIDE + t] * inv * sm[L::OFF_NW + i] * silu(zf);
+        const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + i;
+        if (p.out_f32)
+          static_cast<float*>(p.out)[oi] = y;
+        else
+          static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(y);
+      }
     }
   }
 }
