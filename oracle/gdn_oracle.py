@@ -30,8 +30,10 @@ time, in the order the pages give it:
       Qwen3.8 Flash runtime fixes", commits on recurrent snapshot planes and on
       restoring full checkpoints)
 
-and the same step over a token tree (DDTree-style window: each node continues its
-parent's state and conv history; lucebox #637, ``ggml_ssm_conv_tree``).
+the same step over a token tree (DDTree-style window: each node continues its
+parent's state and conv history; lucebox #637, ``ggml_ssm_conv_tree``), and the
+prefill of whole prompts through the same recurrence (atlas #258 and #297 name the
+prefill GDN paths, VARLEN-FLA / FlashInfer-GDN: ragged prompts packed token-major).
 
 Readings taken where the pages are silent (each is also listed in the design
 notes): taps are a cross-correlation with w[c, W-1] on the current token; no
@@ -297,3 +299,45 @@ def gated_rms_norm(o, z, weight, eps: float = 1e-6):
     z = np.asarray(z, np.float64)
     w = np.asarray(weight, np.float64)
     return o / np.sqrt(np.mean(o * o, axis=-1, keepdims=True) + eps) * w * silu(z)
+
+
+def prefill(dims, cu_seqlens, x, a, b, A_log, dt_bias, conv_w, conv_state, state,
+            q_scale: float = 1.0, l2_eps: float = 1e-6, block: int = 64):
+    """a1..a4 over whole prompts: B prompts of ragged lengths packed token-major
+    (prompt i holds rows cu_seqlens[i] .. cu_seqlens[i+1]-1 of x, a, b and out).
+
+    x [N, C], a, b [N, Hv] (the bf16 values as floats); conv_state [B, W-1, C];
+    state [B, Hv, dv, dk].  Every token takes the plain per-token update of a1..a4;
+    tokens are fed in blocks of `block` only to bound the memory held, the state and
+    conv history carried from one block to the next.  Only the final state and
+    history of each prompt are kept.  Returns a dict with
+      out            [N, Hv, dv]
+      state_out      [B, Hv, dv, dk]
+      conv_state_out [B, W-1, C]
+    An empty prompt leaves its state and history as they were.
+    """
+    cu = np.asarray(cu_seqlens, np.int64)
+    x = np.asarray(x, np.float64)
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    B = cu.shape[0] - 1
+    N = x.shape[0]
+    if cu[0] != 0 or cu[-1] != N or np.any(np.diff(cu) < 0):
+        raise ValueError("cu_seqlens must start at 0, end at N and not decrease")
+    Hv, dv = dims.Hv, dims.dv
+    out = np.zeros((N, Hv, dv))
+    state_out = np.array(state, dtype=np.float64, copy=True)
+    conv_out = np.array(conv_state, dtype=np.float64, copy=True)
+    for i in range(B):
+        hist = conv_out[i:i + 1]
+        S = state_out[i:i + 1]
+        for t0 in range(int(cu[i]), int(cu[i + 1]), block):
+            t1 = min(t0 + block, int(cu[i + 1]))
+            r = verify_step(dims, x[None, t0:t1], a[None, t0:t1], b[None, t0:t1], A_log, dt_bias, conv_w,
+                            hist, S, q_scale=q_scale, l2_eps=l2_eps)
+            out[t0:t1] = r["out"][0]
+            S = r["state_out"]
+            hist = r["conv_state_out"]
+        state_out[i] = S[0]
+        conv_out[i] = hist[0]
+    return {"out": out, "state_out": state_out, "conv_state_out": conv_out}

@@ -453,3 +453,91 @@ def test_gated_norm_scale_invariance_and_unit_rms():
     # the gate enters through SiLU only: z -> large makes the gate the identity on z
     big = O.gated_rms_norm(o, np.full_like(z, 40.0), np.ones(128), eps=0.0)
     np.testing.assert_allclose(big, 40.0 * o / np.sqrt(np.mean(o ** 2, axis=-1, keepdims=True)), rtol=1e-13)
+
+
+# ---------------------------------------------------------------- prefill (whole prompts, packed)
+def _prefill_problem(seed, lens, Hk=2, Hv=4, dk=8, dv=6, dists=Dists()):
+    """Ragged prompts packed token-major, with the per-prompt state and history."""
+    B, N = len(lens), int(sum(lens))
+    d = Dims(B=B, K=1, Hk=Hk, Hv=Hv, dk=dk, dv=dv)
+    g = Gen(seed)
+    lay = make_layer(g, d, dists)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    x = g.normal((N, d.C), 1.0)
+    a = g.normal((N, Hv), 1.0)
+    b = g.normal((N, Hv), 1.0)
+    return d, lay, cu, x, a, b
+
+
+def _prefill(d, lay, cu, x, a, b, state=None, conv=None, block=64):
+    return O.prefill(d, cu, x, a, b, lay.A_log, lay.dt_bias, lay.conv_w,
+                     lay.conv_state if conv is None else conv, lay.state if state is None else state,
+                     q_scale=0.9, block=block)
+
+
+def test_prefill_is_independent_of_the_token_block():
+    """Feeding the prompt in blocks of 64, 5 or 1 tokens does the same per-token arithmetic,
+    so the results agree bit for bit: the state and history are carried across blocks."""
+    d, lay, cu, x, a, b = _prefill_problem(31, [23, 9])
+    r64 = _prefill(d, lay, cu, x, a, b, block=64)
+    for blk in (5, 1):
+        r = _prefill(d, lay, cu, x, a, b, block=blk)
+        for key in ("out", "state_out", "conv_state_out"):
+            np.testing.assert_array_equal(r[key], r64[key])
+
+
+def test_prefill_packing_equals_prompts_alone():
+    lens = [7, 0, 13, 2, 1]
+    d, lay, cu, x, a, b = _prefill_problem(32, lens)
+    r = _prefill(d, lay, cu, x, a, b)
+    for i in range(len(lens)):
+        s, e = int(cu[i]), int(cu[i + 1])
+        d1 = Dims(B=1, K=1, Hk=d.Hk, Hv=d.Hv, dk=d.dk, dv=d.dv)
+        r1 = O.prefill(d1, [0, e - s], x[s:e], a[s:e], b[s:e], lay.A_log, lay.dt_bias, lay.conv_w,
+                       lay.conv_state[i:i + 1], lay.state[i:i + 1], q_scale=0.9)
+        np.testing.assert_array_equal(r["out"][s:e], r1["out"])
+        np.testing.assert_array_equal(r["state_out"][i], r1["state_out"][0])
+        np.testing.assert_array_equal(r["conv_state_out"][i], r1["conv_state_out"][0])
+
+
+def test_prefill_empty_prompt_keeps_state_and_history():
+    d, lay, cu, x, a, b = _prefill_problem(33, [0, 4])
+    r = _prefill(d, lay, cu, x, a, b)
+    np.testing.assert_array_equal(r["state_out"][0], lay.state[0])
+    np.testing.assert_array_equal(r["conv_state_out"][0], lay.conv_state[0])
+
+
+def test_prefill_split_prompt_equals_one_call():
+    """A prompt prefilled in two calls, the second starting from the first's state and
+    history, equals one call over the whole prompt."""
+    d, lay, cu, x, a, b = _prefill_problem(34, [30])
+    whole = _prefill(d, lay, cu, x, a, b)
+    first = _prefill(d, lay, np.array([0, 12]), x[:12], a[:12], b[:12])
+    second = _prefill(d, lay, np.array([0, 18]), x[12:], a[12:], b[12:], state=first["state_out"],
+                      conv=first["conv_state_out"])
+    np.testing.assert_allclose(np.concatenate([first["out"], second["out"]]), whole["out"], rtol=0, atol=0)
+    np.testing.assert_array_equal(second["state_out"], whole["state_out"])
+    np.testing.assert_array_equal(second["conv_state_out"], whole["conv_state_out"])
+
+
+def test_prefill_zero_input_tail_is_pure_decay():
+    """Once the W-1 history rows have left the conv window, an all-zero input has q = k = v = 0:
+    the outputs vanish and the state only decays, S_T = (prod of g over those tokens) S."""
+    lens = [70]
+    d, lay, cu, x, a, b = _prefill_problem(35, lens)
+    x[:] = 0.0
+    r = _prefill(d, lay, cu, x, a, b)
+    W = d.W
+    head = _prefill(d, lay, np.array([0, W - 1]), x[:W - 1], a[:W - 1], b[:W - 1])
+    _, g = O.raw_gates(a[W - 1:], b[W - 1:], lay.A_log, lay.dt_bias)
+    decay = np.prod(g, axis=0)                                   # [Hv]
+    np.testing.assert_allclose(r["state_out"][0], decay[:, None, None] * head["state_out"][0], rtol=1e-12, atol=0)
+    assert np.all(r["out"][W - 1:] == 0.0)
+    assert np.all(r["conv_state_out"][0] == 0.0)
+
+
+def test_prefill_rejects_bad_seqlens():
+    d, lay, cu, x, a, b = _prefill_problem(36, [4, 4])
+    for bad in ([0, 5, 4], [1, 4, 8], [0, 4, 7]):
+        with pytest.raises(ValueError):
+            _prefill(d, lay, np.array(bad), x, a, b)
