@@ -61,6 +61,7 @@ typedef enum {
 #define GDN_DEVERR_ACCEPT_RANGE 2u /* rollback saw an accept length outside 0..K; that sequence was left as is */
 #define GDN_DEVERR_NO_SNAPSHOT 4u  /* rollback saw accept length 0 with no snapshot; that sequence was left as is */
 #define GDN_DEVERR_TREE_PARENT 8u  /* a token tree had a parent outside -1..t-1; it was read as -1 */
+#define GDN_DEVERR_SEQLENS 16u     /* gdn_prefill's cu_seqlens were not 0 = c_0 <= ... <= c_B = n_tokens; nothing was written */
 
 typedef struct {
   int32_t B;       /* sequences */
@@ -228,6 +229,48 @@ gdn_status gdn_verify_step_static_scratch(const gdn_dims* dims, const uint16_t* 
                                           const float* conv_w, const float* conv_state_in, float* conv_state_out,
                                           float* conv_inter, const float* state_in, float* state_out,
                                           float* state_inter, void* out, gdn_stream_t stream);
+
+/*
+ * Prefill of whole prompts: a1..a4 over B prompts of any length, packed
+ * token-major (the VARLEN-FLA / FlashInfer-GDN prefill paths named in atlas
+ * #258 and #297; lucebox #637 speaks of long prefills through the same layer).
+ * The result equals the per-token recurrence of gdn_verify_step run over each
+ * prompt from its state and history; no intermediates are kept.  Prompt i holds
+ * tokens cu_seqlens[i] .. cu_seqlens[i+1]-1 of the packed tensors.
+ *   dims              B = prompts (0..65535), Hk, Hv, dk, dv, conv_w, q_scale,
+ *                     l2_eps, out_f32 as for gdn_verify_step; dims->K is not read
+ *   n_tokens          N, 0 <= N < 2^31: the packed token count
+ *   cu_seqlens_dev    [B + 1] int32 on the device, 4-byte aligned:
+ *                     0 = c_0 <= c_1 <= ... <= c_B = N.  Checked on the device:
+ *                     otherwise GDN_DEVERR_SEQLENS is set and nothing is written.
+ *   x                 [N, C] bf16; a, b [N, Hv] bf16 (may be NULL when N == 0)
+ *   A_log, dt_bias    [Hv] f32; conv_w [C, W] f32
+ *   conv_state_in/out [B, W-1, C] f32: history before / after each prompt; may
+ *                     be the same buffer (in place), else no overlap
+ *   state_in/out      [B, Hv, dv, dk] f32: state before / after each prompt;
+ *                     may be the same buffer (in place), else no overlap
+ *   out               [N, Hv, dv] bf16 or f32 (may be NULL when N == 0)
+ *   workspace         at least gdn_prefill_workspace_size() bytes, 16-byte
+ *                     aligned, no initialisation needed, dead after the call.
+ * An empty prompt passes its state and history through unchanged.
+ * Runs three kernels on `stream`: a one-block check of cu_seqlens that numbers
+ * the 64-token chunks; a per-(chunk, q/k head) kernel, all chunks in parallel
+ * (conv, norms, gates, Gram products and the chunk's 64 x 64 triangular
+ * inverse per v-head); and a per-(prompt, v-head, 32 state rows) kernel that
+ * walks the prompt's chunks in order.
+ */
+gdn_status gdn_prefill(const gdn_dims* dims, int64_t n_tokens, const int32_t* cu_seqlens_dev, const uint16_t* x,
+                       const uint16_t* a, const uint16_t* b, const float* A_log, const float* dt_bias,
+                       const float* conv_w, const float* conv_state_in, float* conv_state_out,
+                       const float* state_in, float* state_out, void* out, void* workspace,
+                       uint64_t workspace_bytes, gdn_stream_t stream);
+
+/*
+ * Bytes of workspace gdn_prefill needs for `dims` (B, Hk, Hv, dk) and N tokens:
+ * with cap = ceil(N / 64) + B chunks,
+ * 16 ceil((B + 5) / 4) + 4 cap (Hk * 128 * dk + Hv * (64 * 65 + 128)).
+ */
+gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int64_t n_tokens, uint64_t* bytes);
 
 /*
  * a5: per sequence, keep the first L = accept_len[b] window tokens

@@ -4,6 +4,7 @@
 // non-OK status always means that nothing ran.  Checks: shapes inside the supported set,
 // 16-byte alignment of every buffer (bulk async copies and float4 accesses need it), the
 // aliasing rules of each call, finite scalars.  See include/gdn.h for the contract.
+#include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -70,10 +71,11 @@ bool overlap(Range a, Range b) { return a.valid() && b.valid() && a.lo < b.hi &&
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-gdn_status check_dims(const gdn_dims* d, bool need_gates) {
+gdn_status check_dims(const gdn_dims* d, bool need_gates, bool check_K = true) {
   if (!d) return fail(GDN_ERR_INVALID_ARG, "dims is NULL");
   if (d->B < 0 || d->B > 65535) return fail(GDN_ERR_INVALID_ARG, "B=%d outside 0..65535", d->B);
-  if (d->K < 1 || d->K > gdn::kKMax) return fail(GDN_ERR_UNSUPPORTED, "K=%d outside 1..%d", d->K, gdn::kKMax);
+  if (check_K && (d->K < 1 || d->K > gdn::kKMax))
+    return fail(GDN_ERR_UNSUPPORTED, "K=%d outside 1..%d", d->K, gdn::kKMax);
   if (d->conv_w != gdn::kConvW) return fail(GDN_ERR_UNSUPPORTED, "conv width %d (only 4)", d->conv_w);
   if (d->Hk < 1 || d->Hv < 1) return fail(GDN_ERR_INVALID_ARG, "Hk=%d Hv=%d must be >= 1", d->Hk, d->Hv);
   if (d->Hv % d->Hk != 0) return fail(GDN_ERR_UNSUPPORTED, "Hv=%d not a multiple of Hk=%d", d->Hv, d->Hk);
@@ -436,6 +438,118 @@ gdn_status gdn_verify_resume(const gdn_dims* dims, const int32_t* accept_len_pre
   v.workspace = workspace;
   v.workspace_bytes = workspace_bytes;
   return verify_impl(dims, v, stream);
+}
+
+gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int64_t n_tokens, uint64_t* bytes) {
+  gdn_status s = check_dims(dims, true, false);
+  if (s != GDN_OK) return s;
+  if (n_tokens < 0 || n_tokens > INT32_MAX) return fail(GDN_ERR_INVALID_ARG, "n_tokens=%lld outside 0..2^31-1", (long long)n_tokens);
+  if (!bytes) return fail(GDN_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = gdn::prefill_workspace_bytes(dims->B, n_tokens, dims->Hk, dims->Hv, dims->dk);
+  return ok();
+}
+
+gdn_status gdn_prefill(const gdn_dims* dims, int64_t n_tokens, const int32_t* cu_seqlens_dev, const uint16_t* x,
+                       const uint16_t* a, const uint16_t* b, const float* A_log, const float* dt_bias,
+                       const float* conv_w, const float* conv_state_in, float* conv_state_out,
+                       const float* state_in, float* state_out, void* out, void* workspace,
+                       uint64_t workspace_bytes, gdn_stream_t stream) {
+  gdn_status s = check_dims(dims, true, false);
+  if (s != GDN_OK) return s;
+  const gdn_dims& d = *dims;
+  if (n_tokens < 0 || n_tokens > INT32_MAX) return fail(GDN_ERR_INVALID_ARG, "n_tokens=%lld outside 0..2^31-1", (long long)n_tokens);
+  if (d.B == 0) {
+    if (n_tokens != 0) return fail(GDN_ERR_INVALID_ARG, "n_tokens=%lld with no prompts", (long long)n_tokens);
+    return ok();
+  }
+  if (!cu_seqlens_dev) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens is NULL");
+  if (reinterpret_cast<uintptr_t>(cu_seqlens_dev) & 3u) return fail(GDN_ERR_INVALID_ARG, "cu_seqlens misaligned");
+  if (n_tokens > 0) {
+    GDN_CHECK_PTR(x, "x");
+    GDN_CHECK_PTR(a, "a");
+    GDN_CHECK_PTR(b, "b");
+    GDN_CHECK_PTR(out, "out");
+  } else {
+    GDN_CHECK_OPT_PTR(x, "x");
+    GDN_CHECK_OPT_PTR(a, "a");
+    GDN_CHECK_OPT_PTR(b, "b");
+    GDN_CHECK_OPT_PTR(out, "out");
+  }
+  GDN_CHECK_PTR(A_log, "A_log");
+  GDN_CHECK_PTR(dt_bias, "dt_bias");
+  GDN_CHECK_PTR(conv_w, "conv_w");
+  GDN_CHECK_PTR(conv_state_in, "conv_state_in");
+  GDN_CHECK_PTR(conv_state_out, "conv_state_out");
+  GDN_CHECK_PTR(state_in, "state_in");
+  GDN_CHECK_PTR(state_out, "state_out");
+  GDN_CHECK_PTR(workspace, "workspace");
+  const size_t ws_need = gdn::prefill_workspace_bytes(d.B, n_tokens, d.Hk, d.Hv, d.dk);
+  if (workspace_bytes < ws_need)
+    return fail(GDN_ERR_INVALID_ARG, "workspace has %llu bytes, needs %zu", (unsigned long long)workspace_bytes, ws_need);
+
+  const size_t C = 2ull * d.Hk * d.dk + size_t(d.Hv) * d.dv;
+  const size_t B = size_t(d.B), N = size_t(n_tokens);
+  const size_t S = size_t(d.Hv) * d.dv * d.dk;
+  const Buf bufs[] = {
+      {"cu_seqlens", range_of(cu_seqlens_dev, (B + 1) * 4), false},
+      {"x", range_of(x, N * C * 2), false},
+      {"a", range_of(a, N * d.Hv * 2), false},
+      {"b", range_of(b, N * d.Hv * 2), false},
+      {"A_log", range_of(A_log, size_t(d.Hv) * 4), false},
+      {"dt_bias", range_of(dt_bias, size_t(d.Hv) * 4), false},
+      {"conv_w", range_of(conv_w, C * 4 * 4), false},
+      {"conv_state_in", range_of(conv_state_in, B * 3 * C * 4), false},
+      {"state_in", range_of(state_in, B * S * 4), false},
+      {"conv_state_out", range_of(conv_state_out, B * 3 * C * 4), true},
+      {"state_out", range_of(state_out, B * S * 4), true},
+      {"out", range_of(out, N * d.Hv * d.dv * (d.out_f32 ? 4 : 2)), true},
+      {"workspace", range_of(workspace, ws_need), true},
+  };
+  const char* in_place[][2] = {{"conv_state_out", "conv_state_in"}, {"state_out", "state_in"}};
+  const int n = int(sizeof(bufs) / sizeof(bufs[0]));
+  for (int i = 0; i < n; ++i) {
+    if (!bufs[i].output) continue;
+    for (int j = 0; j < n; ++j) {
+      if (i == j || (bufs[j].output && j < i) || !overlap(bufs[i].r, bufs[j].r)) continue;
+      bool allowed = false;
+      if (!bufs[j].output && bufs[i].r.lo == bufs[j].r.lo && bufs[i].r.hi == bufs[j].r.hi)
+        for (const auto& pr : in_place)
+          if (!strcmp(pr[0], bufs[i].name) && !strcmp(pr[1], bufs[j].name)) allowed = true;
+      if (!allowed) return fail(GDN_ERR_ALIAS, "%s overlaps %s", bufs[i].name, bufs[j].name);
+    }
+  }
+
+  uint32_t* err = nullptr;
+  s = status_word(&err);
+  if (s != GDN_OK) return s;
+  gdn::PrefillParams p{};
+  p.cu = cu_seqlens_dev;
+  p.x = x;
+  p.a = a;
+  p.b = b;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.conv_w = conv_w;
+  p.conv_state_in = conv_state_in;
+  p.conv_state_out = conv_state_out;
+  p.state_in = state_in;
+  p.state_out = state_out;
+  p.out = out;
+  p.ws = gdn::prefill_workspace_carve(workspace, d.B, n_tokens, d.Hk, d.Hv, d.dk);
+  p.err = err;
+  p.B = d.B;
+  p.Hk = d.Hk;
+  p.Hv = d.Hv;
+  p.dk = d.dk;
+  p.dv = d.dv;
+  p.C = int(C);
+  p.N = n_tokens;
+  p.q_scale = d.q_scale;
+  p.l2_eps = d.l2_eps;
+  p.out_f32 = d.out_f32;
+  cudaError_t e = gdn::launch_prefill(p, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  return ok();
 }
 
 gdn_status gdn_rollback(const gdn_dims* dims, const int32_t* accept_len_dev, const float* state_in_snapshot,

@@ -18,6 +18,7 @@ constexpr uint32_t kDevErrTimeout = GDN_DEVERR_TIMEOUT;
 constexpr uint32_t kDevErrAcceptRange = GDN_DEVERR_ACCEPT_RANGE;
 constexpr uint32_t kDevErrNoSnapshot = GDN_DEVERR_NO_SNAPSHOT;
 constexpr uint32_t kDevErrTreeParent = GDN_DEVERR_TREE_PARENT;
+constexpr uint32_t kDevErrSeqlens = GDN_DEVERR_SEQLENS;
 
 // Upper bound on any spin in device code, in nanoseconds of %globaltimer.
 constexpr uint64_t kSpinLimitNs = 1000000000ull;   // 1 s

@@ -95,6 +95,51 @@ struct RollbackParams {
   long long conv_elems;   // per sequence: (W-1)*C
 };
 
+// ---- chunked prefill (gdn_prefill)
+constexpr int kPrefillChunk = 64;  // tokens per chunk
+
+// Upper bound on the chunks of B prompts holding N tokens in all.
+inline long long prefill_chunk_cap(int B, long long N) { return (N + kPrefillChunk - 1) / kPrefillChunk + B; }
+
+// Prefill workspace:
+//   meta [4 + B + 1] int32   valid flag, chunk count, -, -, first chunk of each prompt (+ total)
+//   kq   [cap][Hk][2][64][dk] normalised k^ then q^ per chunk, token-major, float4-swizzled
+//   wm   [cap][Hv][64][65]    W on and below the diagonal, MQ^T shifted one column right above it
+//   gd   [cap][Hv][2][64]     Gamma_t, then d_t = prod_{t<m<64} g_m
+struct PrefillWorkspace {
+  int32_t* meta;
+  float* kq;
+  float* wm;
+  float* gd;
+  long long chunk_cap;
+};
+
+size_t prefill_workspace_bytes(int B, long long N, int Hk, int Hv, int dk);
+PrefillWorkspace prefill_workspace_carve(void* base, int B, long long N, int Hk, int Hv, int dk);
+
+struct PrefillParams {
+  const int32_t* cu;  // [B + 1] token offsets of the prompts
+  const uint16_t* x;  // [N, C] bf16
+  const uint16_t* a;  // [N, Hv] bf16
+  const uint16_t* b;
+  const float* A_log;
+  const float* dt_bias;
+  const float* conv_w;
+  const float* conv_state_in;  // [B, W-1, C]
+  float* conv_state_out;
+  const float* state_in;  // [B, Hv, dv, dk]
+  float* state_out;
+  void* out;  // [N, Hv, dv]
+  PrefillWorkspace ws;
+  uint32_t* err;
+  int B, Hk, Hv, dk, dv, C;
+  long long N;
+  float q_scale, l2_eps;
+  int out_f32;
+};
+
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
+
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream);
 cudaError_t launch_conv(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_rollback(const RollbackParams& p, cudaStream_t stream);

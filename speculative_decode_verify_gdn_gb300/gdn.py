@@ -15,13 +15,13 @@ import torch
 from .build import LIB_PATH
 
 EXPORTED = ("gdn_conv_step", "gdn_verify_step", "gdn_verify_resume", "gdn_verify_tree", "gdn_verify_gated",
-            "gdn_verify_workspace_size", "gdn_verify_step_static_scratch", "gdn_rollback", "gdn_device_status",
-            "gdn_last_error")
+            "gdn_verify_workspace_size", "gdn_verify_step_static_scratch", "gdn_prefill", "gdn_prefill_workspace_size",
+            "gdn_rollback", "gdn_device_status", "gdn_last_error")
 
 GDN_OK, GDN_ERR_INVALID_ARG, GDN_ERR_UNSUPPORTED, GDN_ERR_ALIAS, GDN_ERR_NO_SNAPSHOT, GDN_ERR_CUDA = range(6)
 STATUS_NAMES = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIAS",
                 4: "GDN_ERR_NO_SNAPSHOT", 5: "GDN_ERR_CUDA"}
-DEVERR_TIMEOUT, DEVERR_ACCEPT_RANGE, DEVERR_NO_SNAPSHOT, DEVERR_TREE_PARENT = 1, 2, 4, 8
+DEVERR_TIMEOUT, DEVERR_ACCEPT_RANGE, DEVERR_NO_SNAPSHOT, DEVERR_TREE_PARENT, DEVERR_SEQLENS = 1, 2, 4, 8, 16
 
 
 class GdnDims(ctypes.Structure):
@@ -64,13 +64,16 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.gdn_verify_tree.argtypes = [D] + [P] * 15 + [ctypes.c_uint64, P]
     lib.gdn_verify_gated.argtypes = [D] + [P] * 14 + [ctypes.c_float, P, P, ctypes.c_uint64, P]
     lib.gdn_verify_workspace_size.argtypes = [D, ctypes.POINTER(ctypes.c_uint64)]
+    lib.gdn_prefill.argtypes = [D, ctypes.c_int64] + [P] * 13 + [ctypes.c_uint64, P]
+    lib.gdn_prefill_workspace_size.argtypes = [D, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint64)]
     lib.gdn_verify_step_static_scratch.argtypes = [D] + [P] * 14
     lib.gdn_rollback.argtypes = [D] + [P] * 8
     lib.gdn_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32, P]
     lib.gdn_last_error.argtypes = []
     lib.gdn_last_error.restype = ctypes.c_char_p
     for f in ("gdn_conv_step", "gdn_verify_step", "gdn_verify_resume", "gdn_verify_tree", "gdn_verify_gated",
-              "gdn_verify_workspace_size", "gdn_verify_step_static_scratch", "gdn_rollback", "gdn_device_status"):
+              "gdn_verify_workspace_size", "gdn_verify_step_static_scratch", "gdn_prefill",
+              "gdn_prefill_workspace_size", "gdn_rollback", "gdn_device_status"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -130,6 +133,45 @@ def gdn_verify_workspace_size(dims: GdnDims) -> int:
 def alloc_workspace(dims: GdnDims, device="cuda") -> torch.Tensor:
     """A uint8 device tensor large enough to serve as gdn_verify_step's workspace."""
     return torch.empty(max(16, gdn_verify_workspace_size(dims)), dtype=torch.uint8, device=device)
+
+
+def gdn_prefill_workspace_size(dims: GdnDims, n_tokens: int) -> int:
+    """Bytes of device scratch gdn_prefill needs for B prompts holding n_tokens tokens."""
+    n = ctypes.c_uint64(0)
+    _check(load_library().gdn_prefill_workspace_size(ctypes.byref(dims), ctypes.c_int64(n_tokens), ctypes.byref(n)))
+    return n.value
+
+
+def alloc_prefill_workspace(dims: GdnDims, n_tokens: int, device="cuda") -> torch.Tensor:
+    return torch.empty(max(16, gdn_prefill_workspace_size(dims, n_tokens)), dtype=torch.uint8, device=device)
+
+
+def gdn_prefill(dims: GdnDims, cu_seqlens, x, a, b, A_log, dt_bias, conv_w, conv_state_in, conv_state_out,
+                state_in, state_out, out, workspace, stream=None) -> None:
+    """a1..a4 over whole prompts packed token-major: cu_seqlens [B + 1] int32 (device),
+    x [N, C], a, b [N, Hv] bf16, out [N, Hv, dv]; states and histories per prompt."""
+    d = dims
+    N = int(x.shape[0]) if x is not None else 0
+    C = d.C
+    S = d.Hv * d.dv * d.dk
+    H = d.B * (d.conv_w - 1) * C
+    odt = torch.float32 if d.out_f32 else torch.bfloat16
+    empty = N == 0
+
+    def tok(t, name, dtype, numel):
+        if empty and (t is None or t.numel() == 0):
+            return None
+        return _ptr(t, name, dtype, numel)
+
+    _check(load_library().gdn_prefill(
+        ctypes.byref(d), ctypes.c_int64(N), _ptr(cu_seqlens, "cu_seqlens", torch.int32, d.B + 1),
+        tok(x, "x", torch.bfloat16, N * C), tok(a, "a", torch.bfloat16, N * d.Hv),
+        tok(b, "b", torch.bfloat16, N * d.Hv), _ptr(A_log, "A_log", torch.float32, d.Hv),
+        _ptr(dt_bias, "dt_bias", torch.float32, d.Hv), _ptr(conv_w, "conv_w", torch.float32, C * d.conv_w),
+        _ptr(conv_state_in, "conv_state_in", torch.float32, H), _ptr(conv_state_out, "conv_state_out", torch.float32, H),
+        _ptr(state_in, "state_in", torch.float32, d.B * S), _ptr(state_out, "state_out", torch.float32, d.B * S),
+        tok(out, "out", odt, N * d.Hv * d.dv), _ws_ptr(workspace), ctypes.c_uint64(_ws_bytes(workspace)),
+        _stream(stream)))
 
 
 def gdn_verify_step(dims: GdnDims, x, a, b, A_log, dt_bias, conv_w, conv_state_in, conv_state_out, conv_inter,

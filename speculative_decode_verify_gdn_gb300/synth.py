@@ -167,6 +167,25 @@ def make_output_gate(g: Gen, d: Dims, z_std: float = 1.0, w_std: float = 0.1):
     return z, w
 
 
+@dataclass
+class Prompts:
+    """Ragged prompts packed token-major (prompt i holds rows cu[i] .. cu[i+1]-1)."""
+    cu: np.ndarray           # [B + 1] int32
+    x: np.ndarray            # [N, C] bf16 bits
+    a: np.ndarray            # [N, Hv] bf16 bits
+    b: np.ndarray            # [N, Hv] bf16 bits
+
+
+def make_prompts(g: Gen, d: Dims, lens, dist: Dists) -> Prompts:
+    lens = np.asarray(lens, np.int64)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    N = int(cu[-1])
+    x = f32_to_bf16_bits(g.normal((N, d.C), dist.x_std).astype(np.float32))
+    a = f32_to_bf16_bits(g.normal((N, d.Hv), dist.a_std).astype(np.float32))
+    b = f32_to_bf16_bits(g.normal((N, d.Hv), dist.b_std).astype(np.float32))
+    return Prompts(cu, x, a, b)
+
+
 def make_round(g: Gen, d: Dims, dist: Dists) -> Round:
     x = f32_to_bf16_bits(g.normal((d.B, d.K, d.C), dist.x_std).astype(np.float32))
     a = f32_to_bf16_bits(g.normal((d.B, d.K, d.Hv), dist.a_std).astype(np.float32))

@@ -180,6 +180,42 @@ def test_gated_validation(lib):
     assert "z" in gdn.last_error()
 
 
+def test_prefill_validation(lib):
+    dims = gdn.make_dims(**BASE)
+    N = 100
+
+    def call(n=N, cu="ok", ws=1 << 40, dims=dims, **swap):
+        pt = _ptrs(13)
+        names = ["cu", "x", "a", "b", "A_log", "dt_bias", "conv_w", "conv_state_in", "conv_state_out", "state_in",
+                 "state_out", "out", "workspace"]
+        args = dict(zip(names, pt))
+        if cu is None:
+            args["cu"] = None
+        elif cu == "odd":
+            args["cu"] = ctypes.c_void_p(P + 2)
+        args.update(swap)
+        return lib.gdn_prefill(ctypes.byref(dims), ctypes.c_int64(n), *[args[k] for k in names],
+                               ctypes.c_uint64(ws), None)
+
+    assert call(cu=None) == gdn.GDN_ERR_INVALID_ARG and "cu_seqlens" in gdn.last_error()
+    assert call(cu="odd") == gdn.GDN_ERR_INVALID_ARG
+    assert call(n=-1) == gdn.GDN_ERR_INVALID_ARG
+    assert call(n=1 << 31) == gdn.GDN_ERR_INVALID_ARG
+    assert call(ws=16) == gdn.GDN_ERR_INVALID_ARG and "workspace" in gdn.last_error()
+    assert call(x=None) == gdn.GDN_ERR_INVALID_ARG
+    assert call(state_out=ctypes.c_void_p(P + MB + 16)) == gdn.GDN_ERR_ALIAS        # state_out inside x
+    assert call(conv_state_out=ctypes.c_void_p(P + 11 * MB)) == gdn.GDN_ERR_ALIAS  # conv_state_out == out
+    assert call(dims=gdn.make_dims(**dict(BASE, dk=96))) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(dims=gdn.make_dims(**dict(BASE, B=0))) == gdn.GDN_ERR_INVALID_ARG   # tokens without prompts
+    assert lib.gdn_prefill(ctypes.byref(gdn.make_dims(**dict(BASE, B=0))), ctypes.c_int64(0), *([None] * 13),
+                           ctypes.c_uint64(0), None) == gdn.GDN_OK                   # nothing to do
+    need = ctypes.c_uint64(0)
+    assert lib.gdn_prefill_workspace_size(ctypes.byref(dims), ctypes.c_int64(N), ctypes.byref(need)) == gdn.GDN_OK
+    cap = (N + 63) // 64 + dims.B
+    expect = 16 * ((dims.B + 5 + 3) // 4) + 4 * cap * (dims.Hk * 128 * dims.dk + dims.Hv * (64 * 65 + 128))
+    assert need.value == expect
+
+
 def test_conv_step_validation(lib):
     dims = gdn.make_dims(**BASE)
     pt = _ptrs(5)
