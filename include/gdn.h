@@ -256,8 +256,10 @@ gdn_status gdn_verify_step_static_scratch(const gdn_dims* dims, const uint16_t* 
  * Runs three kernels on `stream`: a one-block check of cu_seqlens that numbers
  * the 64-token chunks; a per-(chunk, q/k head) kernel, all chunks in parallel
  * (conv, norms, gates, Gram products and the chunk's 64 x 64 triangular
- * inverse per v-head); and a per-(prompt, v-head, 32 state rows) kernel that
- * walks the prompt's chunks in order.
+ * inverse per v-head); and a per-(prompt, v-head, 64 state rows) kernel that
+ * walks the prompt's chunks in order on the tensor cores (tcgen05, the state
+ * in tensor memory; every product is three bf16 MMAs over hi/lo operand
+ * pairs, about 2^-16 relative error per product).
  */
 gdn_status gdn_prefill(const gdn_dims* dims, int64_t n_tokens, const int32_t* cu_seqlens_dev, const uint16_t* x,
                        const uint16_t* a, const uint16_t* b, const float* A_log, const float* dt_bias,
@@ -268,7 +270,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, int64_t n_tokens, const int32_t* cu
 /*
  * Bytes of workspace gdn_prefill needs for `dims` (B, Hk, Hv, dk) and N tokens:
  * with cap = ceil(N / 64) + B chunks,
- * 16 ceil((B + 5) / 4) + 4 cap (Hk * 128 * dk + Hv * (64 * 65 + 128)).
+ * 16 ceil((B + 5) / 4) + cap (Hk * 768 * dk + Hv * 33280).
  */
 gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int64_t n_tokens, uint64_t* bytes);
 

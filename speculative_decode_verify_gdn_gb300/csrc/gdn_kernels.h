@@ -101,15 +101,16 @@ constexpr int kPrefillChunk = 64;  // tokens per chunk
 // Upper bound on the chunks of B prompts holding N tokens in all.
 inline long long prefill_chunk_cap(int B, long long N) { return (N + kPrefillChunk - 1) / kPrefillChunk + B; }
 
-// Prefill workspace:
-//   meta [4 + B + 1] int32   valid flag, chunk count, -, -, first chunk of each prompt (+ total)
-//   kq   [cap][Hk][2][64][dk] normalised k^ then q^ per chunk, token-major, float4-swizzled
-//   wm   [cap][Hv][64][65]    W on and below the diagonal, MQ^T shifted one column right above it
-//   gd   [cap][Hv][2][64]     Gamma_t, then d_t = prod_{t<m<64} g_m
+// Prefill workspace (operands for the tensor cores as bf16 hi/lo pairs, each block in the
+// K-major core-matrix layout of 8 rows x 16 bytes):
+//   meta [4 + B + 1] int32     valid flag, chunk count, -, -, first chunk of each prompt (+ total)
+//   kq   [cap][Hk][6][64 x dk] k^ hi, k^ lo, q^ hi, q^ lo as [t][c]; k^ hi, lo as [c][t]
+//   wm   [cap][Hv][4][64 x 64] W hi, W lo, MQ hi, MQ lo as [t][j]
+//   gd   [cap][Hv][2][64] f32  Gamma_t, then d_t = prod_{t<m<64} g_m
 struct PrefillWorkspace {
   int32_t* meta;
-  float* kq;
-  float* wm;
+  uint16_t* kq;
+  uint16_t* wm;
   float* gd;
   long long chunk_cap;
 };

@@ -27,8 +27,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kCh = kPrefillChunk;   // 64 tokens per chunk
-constexpr int kAS = kCh + 1;         // row stride of the packed W | MQ block
-constexpr int kTileRows = 32;        // state rows per state-kernel CTA
+constexpr int kAS = kCh + 1;         // row stride of the chunk kernel's 64 x 64 shared tables
+constexpr int kTileRows = 64;        // state rows per state-kernel CTA (the MMA M)
+constexpr int kKqBlocks = 6;         // k^ hi, lo, q^ hi, lo, k^T hi, lo per (chunk, q/k head)
 
 __device__ __forceinline__ long long min_ll(long long a, long long b) { return a < b ? a : b; }
 
@@ -40,13 +41,6 @@ __device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
 }
 
 __device__ __forceinline__ float gate_beta(float b) { return 1.f / (1.f + expf(-b)); }
-
-// Position (in floats) of element (t, c) of a 64 x DK token-major table: float4 groups are
-// XOR-swizzled with t & 7 so that eight rows read at the same column hit different banks.
-template <int DK>
-__device__ __forceinline__ int swz(int t, int c4) {
-  return t * DK + ((c4 ^ (t & 7)) << 2);
-}
 
 // ------------------------------------------------------------------------------------------
 // Kernel 0: cu_seqlens check and chunk numbering (one CTA of 1024 threads).
@@ -122,7 +116,8 @@ struct ChunkLayout {
   static constexpr int OFF_KK = R_FLOATS;                     // [64][65] k^_t . k^_j
   static constexpr int OFF_QK = OFF_KK + MAT;                 // [64][65] q^_t . k^_j
   static constexpr int OFF_BG = OFF_QK + MAT;                 // beta[64], g[64], Gamma[64]
-  static constexpr int FLOATS = OFF_BG + 3 * kCh;
+  static constexpr int OFF_Y2 = OFF_BG + 3 * kCh;             // [32][33] product temp of the inverse
+  static constexpr int FLOATS = OFF_Y2 + 32 * 33;
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
 };
 
@@ -156,10 +151,13 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       h[m] = (pos >= s0) ? bf16_to_f32(p.x[size_t(pos) * C + gch])
                          : p.conv_state_in[(size_t(i) * 3 + size_t(pos - s0 + 3)) * C + gch];
     }
+    uint16_t xs[kCh];  // all of the channel's loads in flight at once
+#pragma unroll
+    for (int t = 0; t < kCh; ++t) xs[t] = (t < len) ? p.x[size_t(tok0 + t) * C + gch] : uint16_t(0);
     float h0 = h[0], h1 = h[1], h2 = h[2];
-#pragma unroll 8
+#pragma unroll
     for (int t = 0; t < kCh; ++t) {
-      const float xv = (t < len) ? bf16_to_f32(p.x[size_t(tok0 + t) * C + gch]) : 0.f;
+      const float xv = bf16_to_f32(xs[t]);
       const float z = fmaf(w.w, xv, fmaf(w.z, h2, fmaf(w.y, h1, w.x * h0)));
       sY[t * L::YS + ch] = (t < len) ? silu(z) : 0.f;
       h0 = h1;
@@ -186,15 +184,36 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   }
   __syncthreads();
 
-  // normalised k^ and q^ to the workspace, token-major and swizzled: [2][64][DK]
+  // normalised k^ and q^ to the workspace as bf16 hi/lo MMA operands (K-major core-matrix
+  // layout): k^ hi, k^ lo, q^ hi, q^ lo as [t][c] (K = DK), then k^ hi, lo transposed, [c][t]
+  // (K = 64).  Eight consecutive threads fill one 128-byte core matrix.
   {
-    float* dst = p.ws.kq + (size_t(c) * p.Hk + kh) * 2 * kCh * DK;
-    constexpr int C4 = DK / 4;
-    for (int idx = tid; idx < 2 * kCh * C4; idx += kThreads) {
-      const int part = idx / (kCh * C4);           // 0: k^, 1: q^
-      const int t = (idx / C4) % kCh, c4 = idx % C4;
-      const float4 v = *reinterpret_cast<const float4*>(sY + t * L::YS + (part ? 0 : DK) + 4 * c4);
-      *reinterpret_cast<float4*>(dst + size_t(part) * kCh * DK + swz<DK>(t, c4)) = v;
+    uint8_t* dst = reinterpret_cast<uint8_t*>(p.ws.kq) + (size_t(c) * p.Hk + kh) * kKqBlocks * (kCh * DK * 2);
+    constexpr int BLK = kCh * DK * 2;
+    for (int idx = tid; idx < 2 * kCh * (DK / 8); idx += kThreads) {
+      const int part = idx / (kCh * (DK / 8));  // 0: k^, 1: q^
+      const int cm = (idx >> 3) % (kCh * DK / 64), r8 = idx & 7;
+      const int t = (cm / (DK / 8)) * 8 + r8, cb = cm % (DK / 8);
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = sY[t * L::YS + (part ? 0 : DK) + 8 * cb + q];
+      uint4 hi, lo;
+      split8(v, hi, lo);
+      const uint32_t off = kmajor_off(t, 8 * cb, DK);
+      *reinterpret_cast<uint4*>(dst + (2 * part) * BLK + off) = hi;
+      *reinterpret_cast<uint4*>(dst + (2 * part + 1) * BLK + off) = lo;
+    }
+    for (int idx = tid; idx < DK * (kCh / 8); idx += kThreads) {
+      const int cm = idx >> 3, r8 = idx & 7;
+      const int ch = (cm / (kCh / 8)) * 8 + r8, tb = cm % (kCh / 8);
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = sY[(8 * tb + q) * L::YS + DK + ch];
+      uint4 hi, lo;
+      split8(v, hi, lo);
+      const uint32_t off = kmajor_off(ch, 8 * tb, kCh);
+      *reinterpret_cast<uint4*>(dst + 4 * BLK + off) = hi;
+      *reinterpret_cast<uint4*>(dst + 5 * BLK + off) = lo;
     }
   }
 
@@ -218,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
+        for (int bb = 0; bb <= a; ++bb) {  // blocks with bb > a lie above the diagonal: unused
           kk[a][bb] = fmaf(kt[a].x, kj[bb].x, fmaf(kt[a].y, kj[bb].y, fmaf(kt[a].z, kj[bb].z, fmaf(kt[a].w, kj[bb].w, kk[a][bb]))));
           qk[a][bb] = fmaf(qt[a].x, kj[bb].x, fmaf(qt[a].y, kj[bb].y, fmaf(qt[a].z, kj[bb].z, fmaf(qt[a].w, kj[bb].w, qk[a][bb]))));
         }
@@ -269,26 +288,41 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       }
     }
     __syncthreads();
-    float* A = p.ws.wm + (size_t(c) * p.Hv + h) * (kCh * kAS);
+    // per v-head operands: W hi, W lo, MQ hi, MQ lo, each [t][j] (K = 64), zero above the diagonal
+    uint8_t* wq = reinterpret_cast<uint8_t*>(p.ws.wm) + (size_t(c) * p.Hv + h) * (4 * kCh * kCh * 2);
     float* gd = p.ws.gd + (size_t(c) * p.Hv + h) * (2 * kCh);
-    // beta_t D (k.k) strictly below the diagonal; MQ[t][j] = D (q.k) to A[j][t + 1]; Gamma, d
-    for (int idx = tid; idx < kCh * kCh; idx += kThreads) {
-      const int j = idx / kCh, t = idx % kCh;
-      if (j < t) sL[t * kAS + j] = sBeta[t] * sD[t * kAS + j] * sm[L::OFF_KK + t * kAS + j];
-      if (j <= t) A[j * kAS + t + 1] = sD[t * kAS + j] * sm[L::OFF_QK + t * kAS + j];
+    // beta_t D (k.k) strictly below the diagonal; MQ = D (q.k) on and below it; Gamma, d
+    for (int idx = tid; idx < kCh * (kCh / 8); idx += kThreads) {
+      const int cm = idx >> 3, r8 = idx & 7;
+      const int t = (cm >> 3) * 8 + r8, jb = cm & 7;
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int j = 8 * jb + q;
+        if (j < t) sL[t * kAS + j] = sBeta[t] * sD[t * kAS + j] * sm[L::OFF_KK + t * kAS + j];
+        v[q] = (j <= t) ? sD[t * kAS + j] * sm[L::OFF_QK + t * kAS + j] : 0.f;
+      }
+      uint4 hi, lo;
+      split8(v, hi, lo);
+      const uint32_t off = kmajor_off(t, 8 * jb, kCh);
+      *reinterpret_cast<uint4*>(wq + 2 * (kCh * kCh * 2) + off) = hi;
+      *reinterpret_cast<uint4*>(wq + 3 * (kCh * kCh * 2) + off) = lo;
     }
     if (tid < kCh) {
       gd[tid] = sGam[tid];
       gd[kCh + tid] = sD[(kCh - 1) * kAS + tid];
     }
     __syncthreads();
-    // X = (I + L)^-1 by forward substitution, column j by four lanes (m split mod 4); X
-    // overwrites D (each lane reads back only the X entries it wrote itself)
+    // X = (I + L)^-1, blocked: the four 16 x 16 diagonal blocks by forward substitution
+    // (column j by four lanes, m split mod 4; each lane reads back only the X entries it wrote),
+    // then X21 = -X22 L21 X11 for the 16 x 16 and then the 32 x 32 off-diagonal blocks.  X
+    // overwrites D.
     {
       const int j = tid >> 2, part = tid & 3;
+      const int jb = j & ~15;  // first row / column of j's diagonal block
       const unsigned mask = 0xFu << (threadIdx.x & 28);
       if (part == 0) sD[j * kAS + j] = 1.f;
-      for (int t = j + 1; t < kCh; ++t) {
+      for (int t = j + 1; t < jb + 16; ++t) {
         float s = 0.f;
         for (int m = j + part; m < t; m += 4) s = fmaf(sL[t * kAS + m], sD[m * kAS + j], s);
         s += __shfl_xor_sync(mask, s, 1);
@@ -297,58 +331,101 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       }
     }
     __syncthreads();
+    float* sY2 = sm + L::OFF_Y2;
+#pragma unroll 1
+    for (int bs = 16; bs < kCh; bs *= 2) {
+      // blocks of size 2 bs at offsets o = 0, 2 bs, ...: Y = L21 X11, then X21 = -X22 Y
+      const int nblk = kCh / (2 * bs);
+      const int per = bs * bs;  // Y entries of one block
+      for (int idx = tid; idx < nblk * per; idx += kThreads) {
+        const int blk = idx / per, ii = (idx % per) / bs, jj = idx % bs;
+        const int o = 2 * bs * blk;
+        float y = 0.f;
+        for (int k = jj; k < bs; ++k) y = fmaf(sL[(o + bs + ii) * kAS + o + k], sD[(o + k) * kAS + o + jj], y);
+        sY2[(blk * bs + ii) * 33 + jj] = y;
+      }
+      __syncthreads();
+      for (int idx = tid; idx < nblk * per; idx += kThreads) {
+        const int blk = idx / per, ii = (idx % per) / bs, jj = idx % bs;
+        const int o = 2 * bs * blk;
+        float x = 0.f;
+        for (int k = 0; k <= ii; ++k) x = fmaf(sD[(o + bs + ii) * kAS + o + bs + k], sY2[(blk * bs + k) * 33 + jj], x);
+        sD[(o + bs + ii) * kAS + o + jj] = -x;
+      }
+      __syncthreads();
+    }
     // W = X diag(beta) on and below the diagonal
-    for (int idx = tid; idx < kCh * kCh; idx += kThreads) {
-      const int t = idx / kCh, j = idx % kCh;
-      if (j <= t) A[t * kAS + j] = sD[t * kAS + j] * sBeta[j];
+    for (int idx = tid; idx < kCh * (kCh / 8); idx += kThreads) {
+      const int cm = idx >> 3, r8 = idx & 7;
+      const int t = (cm >> 3) * 8 + r8, jb = cm & 7;
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int j = 8 * jb + q;
+        v[q] = (j <= t) ? sD[t * kAS + j] * sBeta[j] : 0.f;
+      }
+      uint4 hi, lo;
+      split8(v, hi, lo);
+      const uint32_t off = kmajor_off(t, 8 * jb, kCh);
+      *reinterpret_cast<uint4*>(wq + off) = hi;
+      *reinterpret_cast<uint4*>(wq + (kCh * kCh * 2) + off) = lo;
     }
     __syncthreads();
   }
 }
 
 // ------------------------------------------------------------------------------------------
-// Kernel 2: per (prompt, v-head, 32 state rows), sequential over the prompt's chunks.
+// Kernel 2: per (prompt, v-head, 64 state rows), sequential over the prompt's chunks, on the
+// tensor cores.  The f32 state lives in TMEM (64 lanes x DK columns, the M = 64 accumulator
+// layout: row m in lane 32 (m / 16) + m % 16).  Each product of the chunk form is three bf16
+// MMAs over hi/lo operand pairs (hi.hi + hi.lo + lo.hi), about 2^-16 relative per product:
+//   P  = S [k^ | q^]^T   (A = S hi/lo in shared memory, B = k^ / q^ hi/lo from kernel 1)
+//   u  = r W^T           (r = v - Gamma o P_k, written by the threads)
+//   o' = u MQ^T          (out = q_scale (Gamma o P_q + o'))
+//   S  = Gamma_63 S + (d o u) k^   (accumulated into the TMEM state, B = k^T hi/lo)
+// Thread roles: one thread issues the MMAs; in the epilogues lanes 0..15 of warp w hold state
+// row 16 (w % 4) + lane, warps w and w + 4 splitting the columns.
 template <int DK>
-struct StateLayout {
-  static constexpr int KQ = 2 * kCh * DK;                     // k^ then q^, swizzled
-  static constexpr int STAGE = KQ + kCh * kAS + 2 * kCh;      // + W|MQ + Gamma, d
-  static constexpr int SS = DK + 4;                           // state tile row stride
-  static constexpr int XS = 36;                               // raw x row stride
-  static constexpr int OFF_ST = 0;                            // two stages
-  static constexpr int OFF_S = 2 * STAGE;                     // [32][SS]
-  static constexpr int OFF_X = OFF_S + kTileRows * SS;        // [67][XS]: 3 history rows, 64 tokens
-  static constexpr int OFF_VRU = OFF_X + ((67 * XS + 3) & ~3);  // [32][65]: v, then r, then u
-  static constexpr int OFF_PQO = OFF_VRU + ((kTileRows * kAS + 3) & ~3);  // [32][65]: S q^, then o
-  static constexpr int OFF_TAP = OFF_PQO + ((kTileRows * kAS + 3) & ~3);  // [32][4] conv taps
-  static constexpr int OFF_BAR = OFF_TAP + kTileRows * 4;     // two mbarriers
-  static constexpr int FLOATS = OFF_BAR + 4;
-  static constexpr size_t BYTES = size_t(FLOATS) * 4;
-  static constexpr uint32_t KQ_BYTES = KQ * 4;
-  static constexpr uint32_t A_BYTES = kCh * kAS * 4;
-  static constexpr uint32_t GD_BYTES = 2 * kCh * 4;
-  static_assert(STAGE % 4 == 0 && (KQ + kCh * kAS) % 4 == 0 && OFF_S % 4 == 0 && OFF_X % 4 == 0, "16-byte alignment");
-  static_assert(A_BYTES % 16 == 0, "bulk copy size");
+struct TcLayout {
+  static constexpr int BLK_KQ = kCh * DK * 2;            // one 64 x DK bf16 operand
+  static constexpr int BLK = kCh * kCh * 2;              // one 64 x 64 bf16 operand
+  static constexpr int OFF_KQ = 0;                       // k^ hi, lo, q^ hi, lo
+  static constexpr int OFF_KT = OFF_KQ + 4 * BLK_KQ;     // k^T hi, lo
+  static constexpr int OFF_W = OFF_KT + 2 * BLK_KQ;      // W hi, lo
+  static constexpr int OFF_MQ = OFF_W + 2 * BLK;         // MQ hi, lo
+  static constexpr int OFF_GD = OFF_MQ + 2 * BLK;        // two buffers of Gamma[64], d[64]
+  static constexpr int OFF_S = OFF_GD + 2 * 2 * kCh * 4; // S hi, lo (64 x DK)
+  static constexpr int OFF_RD = OFF_S + 2 * BLK_KQ;      // r hi, lo; later (d o u) hi, lo
+  static constexpr int OFF_U = OFF_RD + 2 * BLK;         // u hi, lo
+  static constexpr int OFF_X = OFF_U + 2 * BLK;          // raw x [67][64] f32 (3 history rows)
+  static constexpr int OFF_TAP = OFF_X + 67 * kTileRows * 4;  // conv taps [64][4]
+  static constexpr int OFF_BAR = OFF_TAP + kTileRows * 16;    // mbarriers
+  static constexpr int NBAR = 9;
+  static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_TSLOT + 16;
+  static_assert(OFF_TAP % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 };
 
-template <int DK>
-__device__ __forceinline__ void issue_chunk(const PrefillParams& p, float* stage, uint64_t* bar, int c, int kh, int h) {
-  using L = StateLayout<DK>;
-  mbar_arrive_expect_tx(bar, L::KQ_BYTES + L::A_BYTES + L::GD_BYTES);
-  bulk_load(stage, p.ws.kq + (size_t(c) * p.Hk + kh) * L::KQ, L::KQ_BYTES, bar);
-  bulk_load(stage + L::KQ, p.ws.wm + (size_t(c) * p.Hv + h) * (kCh * kAS), L::A_BYTES, bar);
-  bulk_load(stage + L::KQ + kCh * kAS, p.ws.gd + (size_t(c) * p.Hv + h) * (2 * kCh), L::GD_BYTES, bar);
+// TMEM columns
+constexpr uint32_t kColS = 0, kColPk = 128, kColPq = 192, kColU = 256, kColO = 320, kTmemCols = 512;
+// mbarriers
+enum { kBarKQ = 0, kBarKT, kBarW, kBarMQ, kBarGD0, kBarGD1, kBarP, kBarU, kBarOS };
+
+// every thread waits (bounded); true when any thread of the CTA gave up
+__device__ __forceinline__ bool wait_failed(uint64_t* bar, uint32_t parity) {
+  const bool ok = mbar_wait_bounded(bar, parity);
+  return __syncthreads_or(!ok) != 0;
 }
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const PrefillParams p) {
-  using L = StateLayout<DK>;
-  extern __shared__ __align__(128) float sm[];
-  constexpr int kTiles = DV / kTileRows;
-  const int tid = threadIdx.x;
+  using L = TcLayout<DK>;
+  extern __shared__ __align__(128) uint8_t smb[];
+  constexpr int kHalves = DV / kTileRows;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i = blockIdx.y;
-  const int h = blockIdx.x / kTiles;
-  const int tile = blockIdx.x % kTiles;
-  const int r0 = tile * kTileRows;
+  const int h = blockIdx.x / kHalves;
+  const int r0 = (blockIdx.x % kHalves) * kTileRows;
   const int kh = h / (p.Hv / p.Hk);
   if (p.ws.meta[0] == 0) return;
   const int32_t* base = p.ws.meta + 4;
@@ -356,256 +433,375 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
   const long long s0 = p.cu[i], s1 = p.cu[i + 1];
   const size_t C = size_t(p.C);
   const size_t vch0 = size_t(2) * p.Hk * DK + size_t(h) * DV + r0;  // first conv channel of the tile
-  float* sS = sm + L::OFF_S;
-  float* sX = sm + L::OFF_X;
-  float* sVRU = sm + L::OFF_VRU;
-  float* sPQO = sm + L::OFF_PQO;
-  float* sTap = sm + L::OFF_TAP;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);
+  float* sX = reinterpret_cast<float*>(smb + L::OFF_X);
+  float* sTap = reinterpret_cast<float*>(smb + L::OFF_TAP);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smb + L::OFF_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smb + L::OFF_TSLOT);
+  const uint32_t sbase = smem_addr(smb);
+
+  // epilogue coordinates: row m of the tile (lanes 0..15), column half hh
+  const int quad = warp & 3, hh = warp >> 2;
+  const int m = 16 * quad + (lane & 15);
+  const bool act = lane < 16;
+  const uint32_t lane_sel = uint32_t(32 * quad) << 16;
 
   if (tid == 0) {
-    mbar_init(bar, 1);
-    mbar_init(bar + 1, 1);
+    for (int q = 0; q < L::NBAR; ++q) mbar_init(bar + q, 1);
     fence_mbar_init();
   }
+  if (warp == 0) tmem_alloc(tslot, kTmemCols);
+  tc_fence_before();
   __syncthreads();
-  if (tid == 0) {
-    for (int q = 0; q < 2 && q < n_chunks; ++q) issue_chunk<DK>(p, sm + q * L::STAGE, bar + q, c_first + q, kh, h);
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  // phases armed per barrier (thread 0 only), so that a failed CTA can wait for what it started
+  int armed[L::NBAR] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+  auto issue_kq = [&](int c) {
+    ++armed[kBarKQ];
+    mbar_arrive_expect_tx(bar + kBarKQ, 4 * L::BLK_KQ);
+    bulk_load(smb + L::OFF_KQ, reinterpret_cast<const uint8_t*>(p.ws.kq) + (size_t(c) * p.Hk + kh) * kKqBlocks * L::BLK_KQ,
+              4 * L::BLK_KQ, bar + kBarKQ);
+  };
+  auto issue_kt = [&](int c) {
+    ++armed[kBarKT];
+    mbar_arrive_expect_tx(bar + kBarKT, 2 * L::BLK_KQ);
+    bulk_load(smb + L::OFF_KT,
+              reinterpret_cast<const uint8_t*>(p.ws.kq) + (size_t(c) * p.Hk + kh) * kKqBlocks * L::BLK_KQ + 4 * L::BLK_KQ,
+              2 * L::BLK_KQ, bar + kBarKT);
+  };
+  auto wq_src = [&](int c) {
+    return reinterpret_cast<const uint8_t*>(p.ws.wm) + (size_t(c) * p.Hv + h) * (4 * L::BLK);
+  };
+  auto issue_w = [&](int c) {
+    ++armed[kBarW];
+    mbar_arrive_expect_tx(bar + kBarW, 2 * L::BLK);
+    bulk_load(smb + L::OFF_W, wq_src(c), 2 * L::BLK, bar + kBarW);
+  };
+  auto issue_mq = [&](int c) {
+    ++armed[kBarMQ];
+    mbar_arrive_expect_tx(bar + kBarMQ, 2 * L::BLK);
+    bulk_load(smb + L::OFF_MQ, wq_src(c) + 2 * L::BLK, 2 * L::BLK, bar + kBarMQ);
+  };
+  auto issue_gd = [&](int lc) {  // buffer lc & 1 holds local chunk lc
+    const int b = lc & 1, c = c_first + lc;
+    ++armed[kBarGD0 + b];
+    mbar_arrive_expect_tx(bar + kBarGD0 + b, 2 * kCh * 4);
+    bulk_load(smb + L::OFF_GD + b * 2 * kCh * 4, p.ws.gd + (size_t(c) * p.Hv + h) * (2 * kCh), 2 * kCh * 4,
+              bar + kBarGD0 + b);
+  };
+  if (tid == 0 && n_chunks > 0) {
+    issue_kq(c_first);
+    issue_kt(c_first);
+    issue_w(c_first);
+    issue_mq(c_first);
+    issue_gd(0);
+    if (n_chunks > 1) issue_gd(1);
   }
-  // state tile, conv taps and the three history rows of the tile's v channels
+
+  // S hi/lo operand stores of this thread's columns [c0, c0 + n) of row m
+  auto store_pair = [&](int off, int row, int k0, int kdim, const float* v, int n) {
+    for (int q = 0; q < n; q += 8) {
+      uint4 hi, lo;
+      split8(v + q, hi, lo);
+      const uint32_t o = kmajor_off(row, k0 + q, kdim);
+      *reinterpret_cast<uint4*>(smb + off + o) = hi;
+      *reinterpret_cast<uint4*>(smb + off + (kdim == DK ? L::BLK_KQ : L::BLK) + o) = lo;
+    }
+  };
+
+  // the state tile into TMEM and, split, into the S operand; taps; the v channels' history
+  constexpr int SC = DK / 2;  // state columns per thread
   {
-    const float* src = p.state_in + ((size_t(i) * p.Hv + h) * DV + r0) * DK;
-    for (int idx = tid; idx < kTileRows * DK / 4; idx += kThreads) {
-      const int row = idx / (DK / 4), c4 = idx % (DK / 4);
-      *reinterpret_cast<float4*>(sS + row * L::SS + 4 * c4) = *reinterpret_cast<const float4*>(src + size_t(row) * DK + 4 * c4);
+    const float* src = p.state_in + ((size_t(i) * p.Hv + h) * DV + r0 + m) * DK + hh * SC;
+#pragma unroll
+    for (int c0 = 0; c0 < SC; c0 += 16) {
+      float v[16];
+#pragma unroll
+      for (int q = 0; q < 16; q += 4) {
+        float4 f = act ? *reinterpret_cast<const float4*>(src + c0 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v[q] = f.x; v[q + 1] = f.y; v[q + 2] = f.z; v[q + 3] = f.w;
+      }
+      tmem_st16(tmem + lane_sel + kColS + hh * SC + c0, v);
+      if (act) store_pair(L::OFF_S, m, hh * SC + c0, DK, v, 16);
     }
     if (tid < kTileRows) *reinterpret_cast<float4*>(sTap + 4 * tid) = *reinterpret_cast<const float4*>(p.conv_w + (vch0 + tid) * kConvW);
-    if (tid < 3 * kTileRows) {
-      const int m = tid / kTileRows, ch = tid % kTileRows;
-      sX[m * L::XS + ch] = p.conv_state_in[(size_t(i) * 3 + m) * C + vch0 + ch];
+    for (int idx = tid; idx < 3 * kTileRows; idx += kThreads) {
+      const int mm = idx / kTileRows, ch = idx % kTileRows;
+      sX[mm * kTileRows + ch] = p.conv_state_in[(size_t(i) * 3 + mm) * C + vch0 + ch];
     }
   }
-  // raw x of the tile's 32 channels for one chunk: thread = (token tid / 4, 8 channels)
+  // raw x of the tile's 64 channels for one chunk: thread = (token tid / 4, 16 channels)
   const int xt = tid >> 2, xg = tid & 3;
-  uint4 xr = make_uint4(0, 0, 0, 0);
-  if (n_chunks > 0 && xt < min_ll(kCh, s1 - s0))
-    xr = *reinterpret_cast<const uint4*>(p.x + size_t(s0 + xt) * C + vch0 + 8 * xg);
+  uint4 xr0 = make_uint4(0, 0, 0, 0), xr1 = xr0;
+  if (n_chunks > 0 && xt < min_ll(kCh, s1 - s0)) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + size_t(s0 + xt) * C + vch0 + 16 * xg);
+    xr0 = src[0];
+    xr1 = src[1];
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
 
+  const uint32_t id_n64 = umma_idesc_bf16(kTileRows, kCh), id_ndk = umma_idesc_bf16(kTileRows, DK);
+  bool failed = false;
   int len = 0;
-  for (int lc = 0; lc < n_chunks; ++lc) {
-    const int st = lc & 1;
-    float* stage = sm + st * L::STAGE;
-    const float* sK = stage;
-    const float* sQ = stage + kCh * DK;
-    const float* sA = stage + L::KQ;
-    const float* sGam = sA + kCh * kAS;
+  for (int lc = 0; lc < n_chunks && !failed; ++lc) {
+    const uint32_t par = lc & 1;
+    const float* sGam = reinterpret_cast<const float*>(smb + L::OFF_GD + (lc & 1) * 2 * kCh * 4);
     const float* sd = sGam + kCh;
     const long long tok0 = s0 + (long long)lc * kCh;
     len = int(min_ll(kCh, s1 - tok0));
 
-    // raw x of this chunk to rows 3..66; the next chunk's x is fetched meanwhile
+    // (a) raw x of this chunk to rows 3..66; the next chunk's x is fetched meanwhile
     {
-      const uint32_t wv[4] = {xr.x, xr.y, xr.z, xr.w};
-      float* row = sX + (xt + 3) * L::XS + 8 * xg;
+      const uint32_t wv[8] = {xr0.x, xr0.y, xr0.z, xr0.w, xr1.x, xr1.y, xr1.z, xr1.w};
+      float* row = sX + (xt + 3) * kTileRows + 16 * xg;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 8; ++q) {
         row[2 * q] = (xt < len) ? bf16_to_f32(uint16_t(wv[q] & 0xFFFFu)) : 0.f;
         row[2 * q + 1] = (xt < len) ? bf16_to_f32(uint16_t(wv[q] >> 16)) : 0.f;
       }
       const long long nt = tok0 + kCh + xt;
-      if (lc + 1 < n_chunks && nt < s1) xr = *reinterpret_cast<const uint4*>(p.x + size_t(nt) * C + vch0 + 8 * xg);
-    }
-    // the chunk's tables (bounded wait; the outcome is made uniform over the CTA)
-    const bool ok = mbar_wait_bounded(bar + st, (lc >> 1) & 1);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
-        atomicOr(p.err, kDevErrTimeout);
-        (void)mbar_wait_bounded(bar + (st ^ 1), ((lc + 1) >> 1) & 1);  // copies still in flight
-      }
-      return;
-    }
-
-    // a1 for the v channels: v[ch][t] = SiLU(taps . rows t..t+3)
-    {
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int ch = 8 * xg + q;
-        const float4 w = *reinterpret_cast<const float4*>(sTap + 4 * ch);
-        const float z = fmaf(w.w, sX[(xt + 3) * L::XS + ch],
-                             fmaf(w.z, sX[(xt + 2) * L::XS + ch], fmaf(w.y, sX[(xt + 1) * L::XS + ch], w.x * sX[xt * L::XS + ch])));
-        sVRU[ch * kAS + xt] = silu(z);
+      if (lc + 1 < n_chunks && nt < s1) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + size_t(nt) * C + vch0 + 16 * xg);
+        xr0 = src[0];
+        xr1 = src[1];
       }
     }
-    __syncthreads();
-
-    // S [k^ | q^]: thread (part, rb, tb) takes rows rb + 8a, tokens tb + 16b; for k^ the
-    // epilogue forms r = v - Gamma (S k^) in place of v, for q^ it keeps S q^
-    {
-      const int part = tid >> 7, rb = (tid >> 4) & 7, tb = tid & 15;
-      const float* tab = part ? sQ : sK;
-      float acc[4][4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int bb = 0; bb < 4; ++bb) acc[a][bb] = 0.f;
-#pragma unroll 2
-      for (int c4 = 0; c4 < DK / 4; ++c4) {
-        float4 sv[4], kv[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) sv[a] = *reinterpret_cast<const float4*>(sS + (rb + 8 * a) * L::SS + 4 * c4);
-#pragma unroll
-        for (int bb = 0; bb < 4; ++bb) kv[bb] = *reinterpret_cast<const float4*>(tab + swz<DK>(tb + 16 * bb, c4));
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb)
-            acc[a][bb] = fmaf(sv[a].x, kv[bb].x, fmaf(sv[a].y, kv[bb].y, fmaf(sv[a].z, kv[bb].z, fmaf(sv[a].w, kv[bb].w, acc[a][bb]))));
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-          const int row = rb + 8 * a, t = tb + 16 * bb;
-          if (part == 0)
-            sVRU[row * kAS + t] = fmaf(-sGam[t], acc[a][bb], sVRU[row * kAS + t]);
-          else
-            sPQO[row * kAS + t] = acc[a][bb];
+    // (b) P = S [k^ | q^]^T on the tensor cores
+    if (tid == 0) {
+      if (mbar_wait_bounded(bar + kBarKQ, par)) {
+        tc_fence_after();
+        const uint32_t sS = sbase + L::OFF_S, sKQ = sbase + L::OFF_KQ;
+        constexpr uint32_t sbo = (DK / 8) * 128;
+#pragma unroll 1
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t d = tmem + (part ? kColPq : kColPk);
+          const uint32_t bq = sKQ + part * 2 * L::BLK_KQ;
+#pragma unroll 1
+          for (int sp = 0; sp < 3; ++sp) {  // hi.hi, hi.lo, lo.hi
+            const uint32_t a = sS + (sp == 2 ? L::BLK_KQ : 0);
+            const uint32_t b = bq + (sp == 1 ? L::BLK_KQ : 0);
+#pragma unroll 1
+            for (int kk = 0; kk < DK / 16; ++kk)
+              umma_bf16(d, umma_smem_desc(a + kk * 256, 128, sbo), umma_smem_desc(b + kk * 256, 128, sbo), id_n64,
+                        (sp | kk) != 0);
+          }
         }
-      // the last three rows become the next chunk's history (the conv above is done with them)
-      if (tid < 3 * kTileRows && len == kCh) {
-        const int m = tid / kTileRows, ch = tid % kTileRows;
-        sX[m * L::XS + ch] = sX[(kCh + m) * L::XS + ch];
+        umma_commit(bar + kBarP);
+        ++armed[kBarP];
       }
     }
-    __syncthreads();
-
-    // u = W r: thread (row, tg) takes tokens tg + 8k
-    const int urow = tid >> 3, tg = tid & 7;
-    {
-      float u[8];
+    // (b') meanwhile: the conv of this thread's row m (channel m) over its 32 tokens
+    float v[32];
+    __syncthreads();  // sX rows written in (a)
+    if (act) {
+      const float4 w = *reinterpret_cast<const float4*>(sTap + 4 * m);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) u[k] = 0.f;
-      for (int j = 0; j < kCh; ++j) {
-        const float rj = sVRU[urow * kAS + j];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int t = tg + 8 * k;
-          u[k] = fmaf((j <= t) ? sA[t * kAS + j] : 0.f, rj, u[k]);
-        }
+      for (int q = 0; q < 32; ++q) {
+        const int t = 32 * hh + q;
+        const float z = fmaf(w.w, sX[(t + 3) * kTileRows + m],
+                             fmaf(w.z, sX[(t + 2) * kTileRows + m], fmaf(w.y, sX[(t + 1) * kTileRows + m], w.x * sX[t * kTileRows + m])));
+        v[q] = silu(z);
       }
-      __syncthreads();  // every r is read
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sVRU[urow * kAS + tg + 8 * k] = u[k];
     }
-    __syncthreads();
-
-    // o = q_scale (Gamma S q^ + MQ u), in place of S q^
-    {
-      float o[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int t = tg + 8 * k;
-        o[k] = sGam[t] * sPQO[urow * kAS + t];
-      }
-      for (int j = 0; j < kCh; ++j) {
-        const float uj = sVRU[urow * kAS + j];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int t = tg + 8 * k;
-          o[k] = fmaf((j <= t) ? sA[j * kAS + t + 1] : 0.f, uj, o[k]);
-        }
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) sPQO[urow * kAS + tg + 8 * k] = p.q_scale * o[k];
+    const int gdb = kBarGD0 + (lc & 1);
+    if (wait_failed(bar + gdb, (lc >> 1) & 1) || wait_failed(bar + kBarP, par)) {
+      failed = true;
+      break;
     }
-    // S <- Gamma_63 S + sum_t d_t u_t k^_t^T: thread (row, q8) owns float4 columns q8 + 8m
+    tc_fence_after();
+    // (c) r = v - Gamma o P_k -> operand; S <- Gamma_63 S in TMEM (P no longer reads it)
     {
-      constexpr int NF = DK / 32;
-      float4 s[NF];
+      float pk[32];
+      tmem_ld16(tmem + lane_sel + kColPk + 32 * hh, *reinterpret_cast<float(*)[16]>(pk));
+      tmem_ld16(tmem + lane_sel + kColPk + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(pk + 16));
+      if (act) {
+#pragma unroll
+        for (int q = 0; q < 32; ++q) pk[q] = fmaf(-sGam[32 * hh + q], pk[q], v[q]);
+        store_pair(L::OFF_RD, m, 32 * hh, kCh, pk, 32);
+      }
       const float gl = sGam[kCh - 1];
 #pragma unroll
-      for (int m = 0; m < NF; ++m) {
-        const float4 v = *reinterpret_cast<const float4*>(sS + urow * L::SS + 4 * (tg + 8 * m));
-        s[m] = make_float4(gl * v.x, gl * v.y, gl * v.z, gl * v.w);
-      }
-      for (int t = 0; t < kCh; ++t) {
-        const float cu = sd[t] * sVRU[urow * kAS + t];
+      for (int c0 = 0; c0 < SC; c0 += 16) {
+        float sv[16];
+        tmem_ld16(tmem + lane_sel + kColS + hh * SC + c0, sv);
 #pragma unroll
-        for (int m = 0; m < NF; ++m) {
-          const float4 kv = *reinterpret_cast<const float4*>(sK + swz<DK>(t, tg + 8 * m));
-          s[m].x = fmaf(cu, kv.x, s[m].x);
-          s[m].y = fmaf(cu, kv.y, s[m].y);
-          s[m].z = fmaf(cu, kv.z, s[m].z);
-          s[m].w = fmaf(cu, kv.w, s[m].w);
+        for (int q = 0; q < 16; ++q) sv[q] *= gl;
+        tmem_st16(tmem + lane_sel + kColS + hh * SC + c0, sv);
+      }
+      // the last three raw rows become the next chunk's history (the conv is done with them)
+      if (len == kCh)
+        for (int idx = tid; idx < 3 * kTileRows; idx += kThreads) sX[idx] = sX[kCh * kTileRows + idx];
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // (d) u = r W^T
+    if (tid == 0) {
+      if (lc + 1 < n_chunks) issue_kq(c_first + lc + 1);  // the P MMAs are done with k^, q^
+      if (mbar_wait_bounded(bar + kBarW, par)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int sp = 0; sp < 3; ++sp) {
+          const uint32_t a = sbase + L::OFF_RD + (sp == 2 ? L::BLK : 0);
+          const uint32_t b = sbase + L::OFF_W + (sp == 1 ? L::BLK : 0);
+#pragma unroll 1
+          for (int kk = 0; kk < kCh / 16; ++kk)
+            umma_bf16(tmem + kColU, umma_smem_desc(a + kk * 256, 128, 1024), umma_smem_desc(b + kk * 256, 128, 1024),
+                      id_n64, (sp | kk) != 0);
+        }
+        umma_commit(bar + kBarU);
+        ++armed[kBarU];
+      }
+    }
+    if (wait_failed(bar + kBarU, par)) {
+      failed = true;
+      break;
+    }
+    tc_fence_after();
+    {
+      float u[32];
+      tmem_ld16(tmem + lane_sel + kColU + 32 * hh, *reinterpret_cast<float(*)[16]>(u));
+      tmem_ld16(tmem + lane_sel + kColU + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(u + 16));
+      if (act) {
+        store_pair(L::OFF_U, m, 32 * hh, kCh, u, 32);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) u[q] *= sd[32 * hh + q];
+        store_pair(L::OFF_RD, m, 32 * hh, kCh, u, 32);  // r is dead: the u MMAs are done
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    // (e) o' = u MQ^T and S += (d o u) k^
+    if (tid == 0) {
+      if (lc + 1 < n_chunks) issue_w(c_first + lc + 1);
+      if (mbar_wait_bounded(bar + kBarMQ, par) && mbar_wait_bounded(bar + kBarKT, par)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int sp = 0; sp < 3; ++sp) {
+          const uint32_t a = sbase + L::OFF_U + (sp == 2 ? L::BLK : 0);
+          const uint32_t b = sbase + L::OFF_MQ + (sp == 1 ? L::BLK : 0);
+#pragma unroll 1
+          for (int kk = 0; kk < kCh / 16; ++kk)
+            umma_bf16(tmem + kColO, umma_smem_desc(a + kk * 256, 128, 1024), umma_smem_desc(b + kk * 256, 128, 1024),
+                      id_n64, (sp | kk) != 0);
+        }
+#pragma unroll 1
+        for (int sp = 0; sp < 3; ++sp) {
+          const uint32_t a = sbase + L::OFF_RD + (sp == 2 ? L::BLK : 0);
+          const uint32_t b = sbase + L::OFF_KT + (sp == 1 ? L::BLK_KQ : 0);
+#pragma unroll 1
+          for (int kk = 0; kk < kCh / 16; ++kk)
+            umma_bf16(tmem + kColS, umma_smem_desc(a + kk * 256, 128, 1024), umma_smem_desc(b + kk * 256, 128, 1024),
+                      id_ndk, 1u);
+        }
+        umma_commit(bar + kBarOS);
+        ++armed[kBarOS];
+      }
+    }
+    if (wait_failed(bar + kBarOS, par)) {
+      failed = true;
+      break;
+    }
+    tc_fence_after();
+    // outputs, and the new state split into the S operand for the next chunk
+    {
+      float o[32], pq[32];
+      tmem_ld16(tmem + lane_sel + kColO + 32 * hh, *reinterpret_cast<float(*)[16]>(o));
+      tmem_ld16(tmem + lane_sel + kColO + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(o + 16));
+      tmem_ld16(tmem + lane_sel + kColPq + 32 * hh, *reinterpret_cast<float(*)[16]>(pq));
+      tmem_ld16(tmem + lane_sel + kColPq + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(pq + 16));
+      if (act) {
+        const size_t ob = size_t(h) * DV + r0 + m;
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+          const int t = 32 * hh + q;
+          if (t < len) {
+            const float y = p.q_scale * fmaf(sGam[t], pq[q], o[q]);
+            const size_t oi = size_t(tok0 + t) * p.Hv * DV + ob;
+            if (p.out_f32)
+              static_cast<float*>(p.out)[oi] = y;
+            else
+              static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(y);
+          }
         }
       }
 #pragma unroll
-      for (int m = 0; m < NF; ++m) *reinterpret_cast<float4*>(sS + urow * L::SS + 4 * (tg + 8 * m)) = s[m];
-    }
-    __syncthreads();  // stage st is free; o is complete
-
-    if (tid == 0 && lc + 2 < n_chunks) issue_chunk<DK>(p, stage, bar + st, c_first + lc + 2, kh, h);
-    // outputs: thread = (token xt, rows 8 xg .. 8 xg + 7)
-    if (xt < len) {
-      float ov[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) ov[q] = sPQO[(8 * xg + q) * kAS + xt];
-      const size_t oi = size_t(tok0 + xt) * p.Hv * DV + size_t(h) * DV + r0 + 8 * xg;
-      if (p.out_f32) {
-        float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi);
-        o4[0] = make_float4(ov[0], ov[1], ov[2], ov[3]);
-        o4[1] = make_float4(ov[4], ov[5], ov[6], ov[7]);
-      } else {
-        uint4 pk;
-        pk.x = uint32_t(f32_to_bf16(ov[0])) | (uint32_t(f32_to_bf16(ov[1])) << 16);
-        pk.y = uint32_t(f32_to_bf16(ov[2])) | (uint32_t(f32_to_bf16(ov[3])) << 16);
-        pk.z = uint32_t(f32_to_bf16(ov[4])) | (uint32_t(f32_to_bf16(ov[5])) << 16);
-        pk.w = uint32_t(f32_to_bf16(ov[6])) | (uint32_t(f32_to_bf16(ov[7])) << 16);
-        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + oi) = pk;
+      for (int c0 = 0; c0 < SC; c0 += 16) {
+        float sv[16];
+        tmem_ld16(tmem + lane_sel + kColS + hh * SC + c0, sv);
+        if (act) store_pair(L::OFF_S, m, hh * SC + c0, DK, sv, 16);
       }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && lc + 1 < n_chunks) {
+      issue_mq(c_first + lc + 1);
+      issue_kt(c_first + lc + 1);
+      if (lc + 2 < n_chunks) issue_gd(lc + 2);
     }
   }
 
-  // final state tile
-  {
-    float* dst = p.state_out + ((size_t(i) * p.Hv + h) * DV + r0) * DK;
-    for (int idx = tid; idx < kTileRows * DK / 4; idx += kThreads) {
-      const int row = idx / (DK / 4), c4 = idx % (DK / 4);
-      *reinterpret_cast<float4*>(dst + size_t(row) * DK + 4 * c4) = *reinterpret_cast<const float4*>(sS + row * L::SS + 4 * c4);
+  if (failed) {
+    if (tid == 0) {  // one more bounded wait for every copy and MMA group still in flight
+      atomicOr(p.err, kDevErrTimeout);
+      for (int q = 0; q < L::NBAR; ++q)
+        if (armed[q] > 0) (void)mbar_wait_bounded(bar + q, uint32_t(armed[q] - 1) & 1u);
     }
-  }
-  // conv history: the v channels from the last three rows held in shared memory (rows len ..
-  // len + 2 of the last chunk, or the untouched history of an empty prompt)
-  if (tid < 3 * kTileRows) {
-    const int m = tid / kTileRows, ch = tid % kTileRows;
-    p.conv_state_out[(size_t(i) * 3 + m) * C + vch0 + ch] = sX[(len + m) * L::XS + ch];
-  }
-  // the q|k channels of the head group, split over the first v-head's row tiles; every value
-  // is read before this thread writes, and no other thread of this grid reads them
-  if (h % (p.Hv / p.Hk) == 0) {
-    constexpr int kPer = 2 * DK / kTiles;
-    for (int q = tid; q < kPer; q += kThreads) {
-      const int ch = tile * kPer + q;
-      const size_t gch = (ch < DK) ? size_t(kh) * DK + ch : size_t(p.Hk) * DK + size_t(kh) * DK + (ch - DK);
-      float hv[3];
+  } else {
+    // final state from TMEM
+    float* dst = p.state_out + ((size_t(i) * p.Hv + h) * DV + r0 + m) * DK + hh * SC;
 #pragma unroll
-      for (int m = 0; m < 3; ++m) {
-        const long long pos = s1 - 3 + m;
-        hv[m] = (pos >= s0) ? bf16_to_f32(p.x[size_t(pos) * C + gch])
-                            : p.conv_state_in[(size_t(i) * 3 + size_t(pos - s0 + 3)) * C + gch];
+    for (int c0 = 0; c0 < SC; c0 += 16) {
+      float sv[16];
+      tmem_ld16(tmem + lane_sel + kColS + hh * SC + c0, sv);
+      if (act)
+#pragma unroll
+        for (int q = 0; q < 16; q += 4) *reinterpret_cast<float4*>(dst + c0 + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
+    }
+    // conv history: the v channels from the last three raw rows (rows len .. len + 2 of the
+    // last chunk, or the untouched history of an empty prompt)
+    for (int idx = tid; idx < 3 * kTileRows; idx += kThreads) {
+      const int mm = idx / kTileRows, ch = idx % kTileRows;
+      p.conv_state_out[(size_t(i) * 3 + mm) * C + vch0 + ch] = sX[(len + mm) * kTileRows + ch];
+    }
+    // the q|k channels of the head group, split over the first v-head's row tiles; every value
+    // is read before this thread writes, and no other thread of this grid reads them
+    if (h % (p.Hv / p.Hk) == 0) {
+      constexpr int kPer = 2 * DK / kHalves;
+      for (int q = tid; q < kPer; q += kThreads) {
+        const int ch = (r0 / kTileRows) * kPer + q;
+        const size_t gch = (ch < DK) ? size_t(kh) * DK + ch : size_t(p.Hk) * DK + size_t(kh) * DK + (ch - DK);
+        float hv[3];
+#pragma unroll
+        for (int mm = 0; mm < 3; ++mm) {
+          const long long pos = s1 - 3 + mm;
+          hv[mm] = (pos >= s0) ? bf16_to_f32(p.x[size_t(pos) * C + gch])
+                               : p.conv_state_in[(size_t(i) * 3 + size_t(pos - s0 + 3)) * C + gch];
+        }
+#pragma unroll
+        for (int mm = 0; mm < 3; ++mm) p.conv_state_out[(size_t(i) * 3 + mm) * C + gch] = hv[mm];
       }
-#pragma unroll
-      for (int m = 0; m < 3; ++m) p.conv_state_out[(size_t(i) * 3 + m) * C + gch] = hv[m];
     }
   }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 template <int DK, int DV>
 cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   auto k1 = gdn_prefill_chunk_kernel<DK>;
   auto k2 = gdn_prefill_state_kernel<DK, DV>;
-  const size_t b1 = ChunkLayout<DK>::BYTES, b2 = StateLayout<DK>::BYTES;
+  const size_t b1 = ChunkLayout<DK>::BYTES, b2 = TcLayout<DK>::BYTES;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, int(b1));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, int(b2));
@@ -625,7 +821,7 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
 size_t prefill_workspace_bytes(int B, long long N, int Hk, int Hv, int dk) {
   const long long cap = prefill_chunk_cap(B, N);
   const size_t meta = ((size_t(B) + 5 + 3) & ~size_t(3)) * 4;
-  return meta + size_t(cap) * 4 * (size_t(Hk) * 2 * kCh * dk + size_t(Hv) * (kCh * kAS + 2 * kCh));
+  return meta + size_t(cap) * (size_t(Hk) * kKqBlocks * kCh * dk * 2 + size_t(Hv) * (4 * kCh * kCh * 2 + 2 * kCh * 4));
 }
 
 PrefillWorkspace prefill_workspace_carve(void* base, int B, long long N, int Hk, int Hv, int dk) {
@@ -634,10 +830,10 @@ PrefillWorkspace prefill_workspace_carve(void* base, int B, long long N, int Hk,
   char* p = static_cast<char*>(base);
   w.meta = reinterpret_cast<int32_t*>(p);
   p += ((size_t(B) + 5 + 3) & ~size_t(3)) * 4;
-  w.kq = reinterpret_cast<float*>(p);
-  p += size_t(w.chunk_cap) * Hk * 2 * kCh * dk * 4;
-  w.wm = reinterpret_cast<float*>(p);
-  p += size_t(w.chunk_cap) * Hv * kCh * kAS * 4;
+  w.kq = reinterpret_cast<uint16_t*>(p);
+  p += size_t(w.chunk_cap) * Hk * kKqBlocks * kCh * dk * 2;
+  w.wm = reinterpret_cast<uint16_t*>(p);
+  p += size_t(w.chunk_cap) * Hv * 4 * kCh * kCh * 2;
   w.gd = reinterpret_cast<float*>(p);
   return w;
 }
