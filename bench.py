@@ -59,6 +59,88 @@ def verify_bytes(d, out_bytes: int = 2) -> int:
     return d.B * per_seq + per_launch
 
 
+PREFILL_LENS = [8192] * 8  # prompts of the prefill measurement
+
+
+def prefill_mma_flops(n_chunks: int, Hv: int, dk: int, dv: int) -> int:
+    """bf16 tensor-core FLOPs the prefill state kernel issues: per (chunk, v-head, 64 state rows),
+    three MMAs (hi.hi, hi.lo, lo.hi) for each of S [k^|q^]^T (2 x 64 x 64 x dk), u = r W^T and
+    o = u MQ^T (64 x 64 x 64 each) and the state update (64 x dk x 64)."""
+    macs = 3 * (2 * 64 * 64 * dk + 2 * 64 * 64 * 64 + 64 * dk * 64)
+    return 2 * macs * n_chunks * Hv * (dv // 64)
+
+
+def measured_peak_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def run_prefill(args, world, dev, barrier, max_over_ranks):
+    """Prefill of PREFILL_LENS prompts at the serving layer shape through gdn_prefill, inputs
+    resident; tokens/s over `steps` calls after `warmup`."""
+    import torch
+
+    from speculative_decode_verify_gdn_gb300 import gdn
+    from speculative_decode_verify_gdn_gb300.synth import WORKLOADS, Dims, Gen, make_layer, make_prompts
+
+    w = WORKLOADS[WORKLOAD]
+    lens = PREFILL_LENS
+    d = Dims(B=len(lens), K=1, Hk=w.dims.Hk, Hv=w.dims.Hv, dk=w.dims.dk, dv=w.dims.dv)
+    g = Gen(w.seed + 99)
+    lay = make_layer(g, d, w.dists)
+    pr = make_prompts(g, d, lens, w.dists)
+    N = int(pr.cu[-1])
+    dims = gdn.make_dims(d.B, 1, d.Hk, d.Hv, d.dk, d.dv, d.W, 1.0, 1e-6, 0)
+
+    def bf(b):
+        return torch.from_numpy(np.ascontiguousarray(b).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    def f32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+
+    cu = torch.from_numpy(pr.cu).to(dev)
+    x, a, b = bf(pr.x), bf(pr.a), bf(pr.b)
+    S, CS = f32(lay.state), f32(lay.conv_state)
+    Al, dt, cw = f32(lay.A_log), f32(lay.dt_bias), f32(lay.conv_w)
+    out = torch.empty((N, d.Hv, d.dv), dtype=torch.bfloat16, device=dev)
+    ws = gdn.alloc_prefill_workspace(dims, N, dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        gdn.gdn_prefill(dims, cu, x, a, b, Al, dt, cw, CS, CS, S, S, out, ws, stream)
+
+    n = max(3, min(args.steps, 20))
+    for _ in range(args.warmup):
+        call()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        call()
+    e1.record(stream)
+    barrier()
+    ms = max_over_ranks(e0.elapsed_time(e1), world, dev) / n
+    if gdn.gdn_device_status(clear=True):
+        raise RuntimeError("device status flags after the prefill calls")
+    chunks = sum((L + 63) // 64 for L in lens)
+    tf = prefill_mma_flops(chunks, d.Hv, d.dk, d.dv) / (ms * 1e-3) / 1e12
+    peak, kind = measured_peak_tflops()
+    res = {"value": world * N / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "calls": n,
+           "gpu_launches": 3 * n,
+           "workload": f"{len(lens)} prompts x {lens[0]} tokens, Hk={d.Hk} Hv={d.Hv} dk={d.dk} dv={d.dv}, "
+                       "bf16 inputs and outputs, f32 state, in place",
+           "tensor": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                      "peak_source": f"{kind} (MEASURED_PEAKS.json bf16_tflops)",
+                      "what": "bf16 MMA FLOPs of the state kernel over the whole call (all three kernels)"},
+           "what": "gdn_prefill per call: cu_seqlens check, per-chunk q/k kernel, tensor-core state pass"}
+    del ws, out, x
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------ peaks, clocks, profile
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -349,6 +431,8 @@ def run_gdn(args):
     if gdn.gdn_device_status(clear=True):
         raise RuntimeError("device status flags after the gated steps")
 
+    prefill = run_prefill(args, world, dev, barrier, max_over_ranks)
+
     # e2e: inputs from pinned host memory and the output back, inside the timed region
     e2e = None
     if not args.no_e2e:
@@ -412,6 +496,7 @@ def run_gdn(args):
         "zero_copy_rollback": resume,
         "tree_verify": tree,
         "gated_verify": gated,
+        "prefill": prefill,
     }
     if world > 1:
         dist.barrier()
@@ -458,6 +543,20 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_only(args):
+    import torch
+
+    from speculative_decode_verify_gdn_gb300 import gdn
+    from speculative_decode_verify_gdn_gb300.build import build_library
+
+    torch.cuda.set_device(0)
+    build_library()
+    gdn.load_library()
+    dev = torch.device("cuda", 0)
+    res = run_prefill(args, 1, dev, torch.cuda.synchronize, lambda v, world, dev: v)
+    print(json.dumps({"prefill": res}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -468,11 +567,15 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--only", choices=["prefill"], default=None,
+                    help="run one side measurement alone (for profiling) and print its JSON object")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.only == "prefill":
+        run_prefill_only(args)
     else:
         run_gdn(args)
 
