@@ -185,8 +185,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   __syncthreads();
 
   // normalised k^ and q^ to the workspace as bf16 hi/lo MMA operands (K-major core-matrix
-  // layout): k^ hi, k^ lo, q^ hi, q^ lo as [t][c] (K = DK), then k^ hi, lo transposed, [c][t]
-  // (K = 64).  Eight consecutive threads fill one 128-byte core matrix.
+  // layout): k^ hi, q^ hi, k^ lo, q^ lo as [t][c] (K = DK; k^ and q^ adjacent, so that each pair
+  // reads as one 128-row operand), then k^ hi, lo transposed, [c][t] (K = 64).  Eight
+  // consecutive threads fill one 128-byte core matrix.
   {
     uint8_t* dst = reinterpret_cast<uint8_t*>(p.ws.kq) + (size_t(c) * p.Hk + kh) * kKqBlocks * (kCh * DK * 2);
     constexpr int BLK = kCh * DK * 2;
@@ -200,8 +201,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       uint4 hi, lo;
       split8(v, hi, lo);
       const uint32_t off = kmajor_off(t, 8 * cb, DK);
-      *reinterpret_cast<uint4*>(dst + (2 * part) * BLK + off) = hi;
-      *reinterpret_cast<uint4*>(dst + (2 * part + 1) * BLK + off) = lo;
+      *reinterpret_cast<uint4*>(dst + part * BLK + off) = hi;
+      *reinterpret_cast<uint4*>(dst + (2 + part) * BLK + off) = lo;
     }
     for (int idx = tid; idx < DK * (kCh / 8); idx += kThreads) {
       const int cm = idx >> 3, r8 = idx & 7;
@@ -400,7 +401,7 @@ struct TcLayout {
   static constexpr int OFF_X = OFF_U + 2 * BLK;          // raw x [67][64] f32 (3 history rows)
   static constexpr int OFF_TAP = OFF_X + 67 * kTileRows * 4;  // conv taps [64][4]
   static constexpr int OFF_BAR = OFF_TAP + kTileRows * 16;    // mbarriers
-  static constexpr int NBAR = 9;
+  static constexpr int NBAR = 11;
   static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_TSLOT + 16;
   static_assert(OFF_TAP % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
@@ -409,7 +410,7 @@ struct TcLayout {
 // TMEM columns
 constexpr uint32_t kColS = 0, kColPk = 128, kColPq = 192, kColU = 256, kColO = 320, kTmemCols = 512;
 // mbarriers
-enum { kBarKQ = 0, kBarKT, kBarW, kBarMQ, kBarGD0, kBarGD1, kBarP, kBarU, kBarOS };
+enum { kBarKQ = 0, kBarKT, kBarW, kBarMQ, kBarGD0, kBarGD1, kBarPk, kBarPq, kBarU, kBarO, kBarS };
 
 // every thread waits (bounded); true when any thread of the CTA gave up
 __device__ __forceinline__ bool wait_failed(uint64_t* bar, uint32_t parity) {
@@ -456,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
   const uint32_t tmem = *tslot;
 
   // phases armed per barrier (thread 0 only), so that a failed CTA can wait for what it started
-  int armed[L::NBAR] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+  int armed[L::NBAR] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
   auto issue_kq = [&](int c) {
     ++armed[kBarKQ];
     mbar_arrive_expect_tx(bar + kBarKQ, 4 * L::BLK_KQ);
@@ -545,7 +546,32 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
   tc_fence_after();
 
   const uint32_t id_n64 = umma_idesc_bf16(kTileRows, kCh), id_ndk = umma_idesc_bf16(kTileRows, DK);
+  const uint32_t id_n128 = umma_idesc_bf16(kTileRows, 2 * kCh);
+  // the state in TMEM is kept pre-scaled by the current chunk's Gamma_63, so that the update
+  // MMA can accumulate onto it; this thread's 32-column blocks of it:
+  auto scale_state = [&](const float* gam) {
+    const float gl = gam[kCh - 1];
+#pragma unroll
+    for (int c0 = 0; c0 < SC; c0 += 32) {
+      float sv[32];
+      tmem_ld32(tmem + lane_sel + kColS + hh * SC + c0, sv);
+#pragma unroll
+      for (int q = 0; q < 32; ++q) sv[q] *= gl;
+      tmem_st32(tmem + lane_sel + kColS + hh * SC + c0, sv);
+    }
+  };
   bool failed = false;
+  if (n_chunks > 0) {
+    if (wait_failed(bar + kBarGD0, 0)) {
+      failed = true;
+    } else {
+      tc_fence_after();
+      scale_state(reinterpret_cast<const float*>(smb + L::OFF_GD));
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+    }
+  }
   int len = 0;
   for (int lc = 0; lc < n_chunks && !failed; ++lc) {
     const uint32_t par = lc & 1;
@@ -570,33 +596,29 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
         xr1 = src[1];
       }
     }
-    // (b) P = S [k^ | q^]^T on the tensor cores
+    __syncthreads();  // sX rows written
+    // (b) P = S [k^ | q^]^T on the tensor cores (k^ and q^ stacked as one N = 128 operand, the
+    // result in the adjacent P_k | P_q columns), while the threads run the conv of their row m
+    // (channel m) over their 32 tokens
     if (tid == 0) {
       if (mbar_wait_bounded(bar + kBarKQ, par)) {
         tc_fence_after();
         const uint32_t sS = sbase + L::OFF_S, sKQ = sbase + L::OFF_KQ;
         constexpr uint32_t sbo = (DK / 8) * 128;
 #pragma unroll 1
-        for (int part = 0; part < 2; ++part) {
-          const uint32_t d = tmem + (part ? kColPq : kColPk);
-          const uint32_t bq = sKQ + part * 2 * L::BLK_KQ;
+        for (int sp = 0; sp < 3; ++sp) {  // hi.hi, hi.lo, lo.hi
+          const uint32_t a = sS + (sp == 2 ? L::BLK_KQ : 0);
+          const uint32_t b = sKQ + (sp == 1 ? 2 * L::BLK_KQ : 0);
 #pragma unroll 1
-          for (int sp = 0; sp < 3; ++sp) {  // hi.hi, hi.lo, lo.hi
-            const uint32_t a = sS + (sp == 2 ? L::BLK_KQ : 0);
-            const uint32_t b = bq + (sp == 1 ? L::BLK_KQ : 0);
-#pragma unroll 1
-            for (int kk = 0; kk < DK / 16; ++kk)
-              umma_bf16(d, umma_smem_desc(a + kk * 256, 128, sbo), umma_smem_desc(b + kk * 256, 128, sbo), id_n64,
-                        (sp | kk) != 0);
-          }
+          for (int kk = 0; kk < DK / 16; ++kk)
+            umma_bf16(tmem + kColPk, umma_smem_desc(a + kk * 256, 128, sbo), umma_smem_desc(b + kk * 256, 128, sbo),
+                      id_n128, (sp | kk) != 0);
         }
-        umma_commit(bar + kBarP);
-        ++armed[kBarP];
+        umma_commit(bar + kBarPk);
+        ++armed[kBarPk];
       }
     }
-    // (b') meanwhile: the conv of this thread's row m (channel m) over its 32 tokens
     float v[32];
-    __syncthreads();  // sX rows written in (a)
     if (act) {
       const float4 w = *reinterpret_cast<const float4*>(sTap + 4 * m);
 #pragma unroll
@@ -607,30 +629,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
         v[q] = silu(z);
       }
     }
-    const int gdb = kBarGD0 + (lc & 1);
-    if (wait_failed(bar + gdb, (lc >> 1) & 1) || wait_failed(bar + kBarP, par)) {
+    if (wait_failed(bar + kBarPk, par)) {
       failed = true;
       break;
     }
     tc_fence_after();
-    // (c) r = v - Gamma o P_k -> operand; S <- Gamma_63 S in TMEM (P no longer reads it)
+    // (c) r = v - Gamma o P_k -> operand
     {
       float pk[32];
-      tmem_ld16(tmem + lane_sel + kColPk + 32 * hh, *reinterpret_cast<float(*)[16]>(pk));
-      tmem_ld16(tmem + lane_sel + kColPk + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(pk + 16));
+      tmem_ld32(tmem + lane_sel + kColPk + 32 * hh, pk);
       if (act) {
 #pragma unroll
         for (int q = 0; q < 32; ++q) pk[q] = fmaf(-sGam[32 * hh + q], pk[q], v[q]);
         store_pair(L::OFF_RD, m, 32 * hh, kCh, pk, 32);
-      }
-      const float gl = sGam[kCh - 1];
-#pragma unroll
-      for (int c0 = 0; c0 < SC; c0 += 16) {
-        float sv[16];
-        tmem_ld16(tmem + lane_sel + kColS + hh * SC + c0, sv);
-#pragma unroll
-        for (int q = 0; q < 16; ++q) sv[q] *= gl;
-        tmem_st16(tmem + lane_sel + kColS + hh * SC + c0, sv);
       }
       // the last three raw rows become the next chunk's history (the conv is done with them)
       if (len == kCh)
@@ -640,9 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // (d) u = r W^T
+    // (d) u = r W^T; once the q^ MMAs are done too, the next chunk's k^|q^ may come in
     if (tid == 0) {
-      if (lc + 1 < n_chunks) issue_kq(c_first + lc + 1);  // the P MMAs are done with k^, q^
       if (mbar_wait_bounded(bar + kBarW, par)) {
         tc_fence_after();
 #pragma unroll 1
@@ -657,6 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
         umma_commit(bar + kBarU);
         ++armed[kBarU];
       }
+      if (lc + 1 < n_chunks) issue_kq(c_first + lc + 1);  // the P MMAs are done with k^, q^
     }
     if (wait_failed(bar + kBarU, par)) {
       failed = true;
@@ -665,8 +676,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     tc_fence_after();
     {
       float u[32];
-      tmem_ld16(tmem + lane_sel + kColU + 32 * hh, *reinterpret_cast<float(*)[16]>(u));
-      tmem_ld16(tmem + lane_sel + kColU + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(u + 16));
+      tmem_ld32(tmem + lane_sel + kColU + 32 * hh, u);
       if (act) {
         store_pair(L::OFF_U, m, 32 * hh, kCh, u, 32);
 #pragma unroll
@@ -678,10 +688,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // (e) o' = u MQ^T and S += (d o u) k^
+    // (e) o' = u MQ^T (own commit), then S += (d o u) k^
     if (tid == 0) {
       if (lc + 1 < n_chunks) issue_w(c_first + lc + 1);
-      if (mbar_wait_bounded(bar + kBarMQ, par) && mbar_wait_bounded(bar + kBarKT, par)) {
+      if (mbar_wait_bounded(bar + kBarMQ, par)) {
         tc_fence_after();
 #pragma unroll 1
         for (int sp = 0; sp < 3; ++sp) {
@@ -692,6 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
             umma_bf16(tmem + kColO, umma_smem_desc(a + kk * 256, 128, 1024), umma_smem_desc(b + kk * 256, 128, 1024),
                       id_n64, (sp | kk) != 0);
         }
+        umma_commit(bar + kBarO);
+        ++armed[kBarO];
+      }
+      if (mbar_wait_bounded(bar + kBarKT, par)) {
 #pragma unroll 1
         for (int sp = 0; sp < 3; ++sp) {
           const uint32_t a = sbase + L::OFF_RD + (sp == 2 ? L::BLK : 0);
@@ -701,49 +715,80 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
             umma_bf16(tmem + kColS, umma_smem_desc(a + kk * 256, 128, 1024), umma_smem_desc(b + kk * 256, 128, 1024),
                       id_ndk, 1u);
         }
-        umma_commit(bar + kBarOS);
-        ++armed[kBarOS];
+        umma_commit(bar + kBarS);
+        ++armed[kBarS];
       }
     }
-    if (wait_failed(bar + kBarOS, par)) {
-      failed = true;
-      break;
+    {
+      const bool ok = mbar_wait_bounded(bar + kBarO, par);
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        break;
+      }
     }
     tc_fence_after();
-    // outputs, and the new state split into the S operand for the next chunk
+    // outputs, while the state update runs: staged token-major in the u operand buffer (the o'
+    // MMAs are done with it) and written out after the next barrier as 16-byte stores
+    float* sOut = reinterpret_cast<float*>(smb + L::OFF_U);  // [64 tokens][64 rows]
     {
       float o[32], pq[32];
-      tmem_ld16(tmem + lane_sel + kColO + 32 * hh, *reinterpret_cast<float(*)[16]>(o));
-      tmem_ld16(tmem + lane_sel + kColO + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(o + 16));
-      tmem_ld16(tmem + lane_sel + kColPq + 32 * hh, *reinterpret_cast<float(*)[16]>(pq));
-      tmem_ld16(tmem + lane_sel + kColPq + 32 * hh + 16, *reinterpret_cast<float(*)[16]>(pq + 16));
+      tmem_ld32(tmem + lane_sel + kColO + 32 * hh, o);
+      tmem_ld32(tmem + lane_sel + kColPq + 32 * hh, pq);
       if (act) {
-        const size_t ob = size_t(h) * DV + r0 + m;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const int t = 32 * hh + q;
-          if (t < len) {
-            const float y = p.q_scale * fmaf(sGam[t], pq[q], o[q]);
-            const size_t oi = size_t(tok0 + t) * p.Hv * DV + ob;
-            if (p.out_f32)
-              static_cast<float*>(p.out)[oi] = y;
-            else
-              static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(y);
-          }
-        }
+        for (int q = 0; q < 32; ++q) sOut[(32 * hh + q) * kTileRows + m] = p.q_scale * fmaf(sGam[32 * hh + q], pq[q], o[q]);
       }
+    }
+    // the new state: split into the S operand of the next chunk, and pre-scaled in TMEM by the
+    // next chunk's Gamma_63
+    const bool more = lc + 1 < n_chunks;
+    {
+      bool ok = mbar_wait_bounded(bar + kBarS, par);
+      if (more) ok = ok && mbar_wait_bounded(bar + kBarGD0 + ((lc + 1) & 1), ((lc + 1) >> 1) & 1);
+      if (__syncthreads_or(!ok)) {
+        failed = true;
+        break;
+      }
+    }
+    tc_fence_after();
+    if (xt < len) {  // thread = (token xt, rows 16 xg .. 16 xg + 15)
+      const float* src = sOut + xt * kTileRows + 16 * xg;
+      const size_t oi = size_t(tok0 + xt) * p.Hv * DV + size_t(h) * DV + r0 + 16 * xg;
+      if (p.out_f32) {
+        float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi);
 #pragma unroll
-      for (int c0 = 0; c0 < SC; c0 += 16) {
-        float sv[16];
-        tmem_ld16(tmem + lane_sel + kColS + hh * SC + c0, sv);
-        if (act) store_pair(L::OFF_S, m, hh * SC + c0, DK, sv, 16);
+        for (int q = 0; q < 4; ++q) o4[q] = *reinterpret_cast<const float4*>(src + 4 * q);
+      } else {
+        uint32_t w[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const __nv_bfloat162 b2 = __floats2bfloat162_rn(src[2 * q], src[2 * q + 1]);
+          w[q] = *reinterpret_cast<const uint32_t*>(&b2);
+        }
+        uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + oi);
+        o4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        o4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+    }
+    {
+      const float gl = more ? reinterpret_cast<const float*>(smb + L::OFF_GD + ((lc + 1) & 1) * 2 * kCh * 4)[kCh - 1] : 1.f;
+#pragma unroll
+      for (int c0 = 0; c0 < SC; c0 += 32) {
+        float sv[32];
+        tmem_ld32(tmem + lane_sel + kColS + hh * SC + c0, sv);
+        if (act) store_pair(L::OFF_S, m, hh * SC + c0, DK, sv, 32);
+        if (more) {
+#pragma unroll
+          for (int q = 0; q < 32; ++q) sv[q] *= gl;
+          tmem_st32(tmem + lane_sel + kColS + hh * SC + c0, sv);
+        }
       }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0 && lc + 1 < n_chunks) {
+    if (tid == 0 && more) {
       issue_mq(c_first + lc + 1);
       issue_kt(c_first + lc + 1);
       if (lc + 2 < n_chunks) issue_gd(lc + 2);
@@ -760,12 +805,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     // final state from TMEM
     float* dst = p.state_out + ((size_t(i) * p.Hv + h) * DV + r0 + m) * DK + hh * SC;
 #pragma unroll
-    for (int c0 = 0; c0 < SC; c0 += 16) {
-      float sv[16];
-      tmem_ld16(tmem + lane_sel + kColS + hh * SC + c0, sv);
+    for (int c0 = 0; c0 < SC; c0 += 32) {
+      float sv[32];
+      tmem_ld32(tmem + lane_sel + kColS + hh * SC + c0, sv);
       if (act)
 #pragma unroll
-        for (int q = 0; q < 16; q += 4) *reinterpret_cast<float4*>(dst + c0 + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
+        for (int q = 0; q < 32; q += 4) *reinterpret_cast<float4*>(dst + c0 + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
     }
     // conv history: the v channels from the last three raw rows (rows len .. len + 2 of the
     // last chunk, or the untouched history of an empty prompt)
