@@ -25,20 +25,14 @@
 namespace gdn {
 namespace {
 
+__device__ __forceinline__ long long min_ll(long long a, long long b) { return a < b ? a : b; }
+
 constexpr int kThreads = 256;
 constexpr int kCh = kPrefillChunk;   // 64 tokens per chunk
 constexpr int kAS = kCh + 1;         // row stride of the chunk kernel's 64 x 64 shared tables
 constexpr int kTileRows = 64;        // state rows per state-kernel CTA (the MMA M)
 constexpr int kKqBlocks = 6;         // k^ hi, lo, q^ hi, lo, k^T hi, lo per (chunk, q/k head)
-
-__device__ __forceinline__ long long min_ll(long long a, long long b) { return a < b ? a : b; }
-
-__device__ __forceinline__ float gate_g(float a, float A_log, float dt_bias) {
-  const float A = -expf(A_log);
-  const float av = a + dt_bias;
-  const float sp = (av > 20.f) ? av : log1pf(expf(av));
-  return expf(sp * A);
-}
+constexpr int kAbHeads = 8;          // v-heads per q/k head whose gate inputs the chunk kernel prefetches
 
 __device__ __forceinline__ float gate_beta(float b) { return 1.f / (1.f + expf(-b)); }
 
@@ -74,32 +68,24 @@ __global__ void __launch_bounds__(1024) gdn_prefill_index_kernel(const PrefillPa
   }
   int32_t* base = p.ws.meta + 4;
   long long run = tid ? part[tid - 1] : 0;
+  const bool valid = !bad && part[1023] <= p.ws.chunk_cap;
   for (int i = i0; i < i1; ++i) {
     base[i] = int32_t(run);
     const long long s = p.cu[i], e = p.cu[i + 1];
-    if (e >= s) run += (e - s + kCh - 1) / kCh;
+    if (e >= s) {
+      const int n = int((e - s + kCh - 1) / kCh);
+      if (valid)  // one record per chunk: prompt, first token, tokens, first token of the prompt
+        for (int lc = 0; lc < n; ++lc)
+          p.ws.chunks[run + lc] = make_int4(i, int(s) + lc * kCh, int(min_ll(kCh, e - s - lc * kCh)), int(s));
+      run += n;
+    }
   }
   if (tid == 1023) {
-    const bool ok = !bad && part[1023] <= p.ws.chunk_cap;
     base[B] = int32_t(part[1023]);
-    p.ws.meta[1] = ok ? int32_t(part[1023]) : 0;
-    p.ws.meta[0] = ok ? 1 : 0;
-    if (!ok) atomicOr(p.err, kDevErrSeqlens);
+    p.ws.meta[1] = valid ? int32_t(part[1023]) : 0;
+    p.ws.meta[0] = valid ? 1 : 0;
+    if (!valid) atomicOr(p.err, kDevErrSeqlens);
   }
-}
-
-// Prompt i holding global chunk c: the largest i with base[i] <= c (empty prompts share their
-// successor's base, so the largest one is the prompt that owns the chunk).
-__device__ __forceinline__ int prompt_of_chunk(const int32_t* base, int B, int c) {
-  int lo = 0, hi = B - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (base[mid] <= c)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  return lo;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -115,9 +101,10 @@ struct ChunkLayout {
   static constexpr int R_FLOATS = (Y_FLOATS > 2 * MAT) ? Y_FLOATS : 2 * MAT;
   static constexpr int OFF_KK = R_FLOATS;                     // [64][65] k^_t . k^_j
   static constexpr int OFF_QK = OFF_KK + MAT;                 // [64][65] q^_t . k^_j
-  static constexpr int OFF_BG = OFF_QK + MAT;                 // beta[64], g[64], Gamma[64]
+  static constexpr int OFF_BG = OFF_QK + MAT;                 // beta[64], G[64] (sum of log g), Gamma[64]
   static constexpr int OFF_Y2 = OFF_BG + 3 * kCh;             // [32][33] product temp of the inverse
-  static constexpr int FLOATS = OFF_Y2 + 32 * 33;
+  static constexpr int OFF_AB = OFF_Y2 + 32 * 33;             // a, b of the first kAbHeads v-heads [e][2][64]
+  static constexpr int FLOATS = OFF_AB + kAbHeads * 2 * kCh;
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
 };
 
@@ -128,15 +115,21 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   const int tid = threadIdx.x;
   const int c = blockIdx.x;
   const int kh = blockIdx.y;
-  const int32_t* meta = p.ws.meta;
-  if (meta[0] == 0 || c >= meta[1]) return;
-  const int32_t* base = meta + 4;
-  const int i = prompt_of_chunk(base, p.B, c);
-  const long long s0 = p.cu[i], s1 = p.cu[i + 1];
-  const long long tok0 = s0 + (long long)(c - base[i]) * kCh;
-  const int len = int(min_ll(kCh, s1 - tok0));
+  if (c >= p.ws.meta[1]) return;  // (0 when cu_seqlens were rejected)
+  const int4 rec = p.ws.chunks[c];
+  const int i = rec.x, len = rec.z;
+  const long long tok0 = rec.y, s0 = rec.w;
   const size_t C = size_t(p.C);
   const int r = p.Hv / p.Hk;
+
+  // the gate inputs of the group's first v-heads, fetched now so that they arrive during the conv
+  float* sAB = sm + L::OFF_AB;
+  for (int idx = tid; idx < min(r, kAbHeads) * kCh; idx += kThreads) {
+    const int e = idx / kCh, t = idx % kCh;
+    const size_t gi = size_t(tok0 + t) * p.Hv + size_t(kh) * r + e;
+    sAB[(2 * e) * kCh + t] = (t < len) ? bf16_to_f32(p.a[gi]) : 0.f;
+    sAB[(2 * e + 1) * kCh + t] = (t < len) ? bf16_to_f32(p.b[gi]) : 0.f;
+  }
 
   // a1 for the head's 2 DK q|k channels, one thread per channel walking the chunk; the three
   // rows before the chunk come from the prompt itself or, at its start, from the history
@@ -221,11 +214,11 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   // Gram products k^_t . k^_j and q^_t . k^_j: thread (tb, jb) takes t = tb + 16a, j = jb + 16b
   {
     const int tb = tid >> 4, jb = tid & 15;
-    float kk[4][4], qk[4][4];
+    float2 kk[4][4], qk[4][4];  // (even, odd channel) partial sums
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
-      for (int bb = 0; bb < 4; ++bb) kk[a][bb] = qk[a][bb] = 0.f;
+      for (int bb = 0; bb < 4; ++bb) kk[a][bb] = qk[a][bb] = make_float2(0.f, 0.f);
 #pragma unroll 2
     for (int c4 = 0; c4 < DK / 4; ++c4) {
       float4 kt[4], qt[4], kj[4];
@@ -239,16 +232,18 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int bb = 0; bb <= a; ++bb) {  // blocks with bb > a lie above the diagonal: unused
-          kk[a][bb] = fmaf(kt[a].x, kj[bb].x, fmaf(kt[a].y, kj[bb].y, fmaf(kt[a].z, kj[bb].z, fmaf(kt[a].w, kj[bb].w, kk[a][bb]))));
-          qk[a][bb] = fmaf(qt[a].x, kj[bb].x, fmaf(qt[a].y, kj[bb].y, fmaf(qt[a].z, kj[bb].z, fmaf(qt[a].w, kj[bb].w, qk[a][bb]))));
+          kk[a][bb] = __ffma2_rn(make_float2(kt[a].x, kt[a].y), make_float2(kj[bb].x, kj[bb].y), kk[a][bb]);
+          kk[a][bb] = __ffma2_rn(make_float2(kt[a].z, kt[a].w), make_float2(kj[bb].z, kj[bb].w), kk[a][bb]);
+          qk[a][bb] = __ffma2_rn(make_float2(qt[a].x, qt[a].y), make_float2(kj[bb].x, kj[bb].y), qk[a][bb]);
+          qk[a][bb] = __ffma2_rn(make_float2(qt[a].z, qt[a].w), make_float2(kj[bb].z, kj[bb].w), qk[a][bb]);
         }
     }
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int bb = 0; bb < 4; ++bb) {
-        sm[L::OFF_KK + (tb + 16 * a) * kAS + jb + 16 * bb] = kk[a][bb];
-        sm[L::OFF_QK + (tb + 16 * a) * kAS + jb + 16 * bb] = qk[a][bb];
+        sm[L::OFF_KK + (tb + 16 * a) * kAS + jb + 16 * bb] = kk[a][bb].x + kk[a][bb].y;
+        sm[L::OFF_QK + (tb + 16 * a) * kAS + jb + 16 * bb] = qk[a][bb].x + qk[a][bb].y;
       }
   }
   __syncthreads();  // the q|k table is dead from here: its space holds D, X and beta D (k.k)
@@ -256,38 +251,53 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   float* sD = sm + L::OFF_D;  // D[t][j] (j <= t), later X = (I + beta D o KK)^-1
   float* sL = sm + L::OFF_L;
   float* sBeta = sm + L::OFF_BG;
-  float* sG = sBeta + kCh;
+  float* sG = sBeta + kCh;  // log g, then its running sum G
   float* sGam = sG + kCh;
   for (int e = 0; e < r; ++e) {
     const int h = kh * r + e;
-    // a3 for this v-head (padding tokens: beta = 0, g = 1, so they change nothing)
+    // a3 for this v-head (padding tokens: beta = 0, g = 1, so they change nothing); log g =
+    // softplus(a + dt_bias) A is kept, and G_t = sum_{m<=t} log g_m
     if (tid < kCh) {
-      float beta = 0.f, g = 1.f;
+      float beta = 0.f, lg = 0.f;
       if (tid < len) {
-        const size_t gi = size_t(tok0 + tid) * p.Hv + h;
-        g = gate_g(bf16_to_f32(p.a[gi]), p.A_log[h], p.dt_bias[h]);
-        beta = gate_beta(bf16_to_f32(p.b[gi]));
+        float av, bv;
+        if (e < kAbHeads) {
+          av = sAB[(2 * e) * kCh + tid];
+          bv = sAB[(2 * e + 1) * kCh + tid];
+        } else {
+          const size_t gi = size_t(tok0 + tid) * p.Hv + h;
+          av = bf16_to_f32(p.a[gi]);
+          bv = bf16_to_f32(p.b[gi]);
+        }
+        const float A = -expf(p.A_log[h]);
+        const float z = av + p.dt_bias[h];
+        lg = ((z > 20.f) ? z : log1pf(expf(z))) * A;
+        beta = gate_beta(bv);
       }
       sBeta[tid] = beta;
-      sG[tid] = g;
+      sG[tid] = lg;
     }
     __syncthreads();
-    // decay products: column j runs down the rows; thread 64 forms Gamma
-    if (tid < kCh) {
-      const int j = tid;
-      float dcur = 1.f;
-      sD[j * kAS + j] = 1.f;
-      for (int t = j + 1; t < kCh; ++t) {
-        dcur *= sG[t];
-        sD[t * kAS + j] = dcur;
+    if (tid < 32) {  // inclusive scan of log g over the chunk, two tokens per lane
+      const float v0 = sG[2 * tid], v1 = sG[2 * tid + 1];
+      float run = v0 + v1;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, run, o);
+        if (tid >= o) run += n;
       }
-    } else if (tid == kCh) {
-      float gam = 1.f;
-      for (int t = 0; t < kCh; ++t) {
-        gam *= sG[t];
-        sGam[t] = gam;
-      }
+      __syncwarp();
+      sG[2 * tid] = run - v1;
+      sG[2 * tid + 1] = run;
     }
+    __syncthreads();
+    // decay products D[t][j] = prod_{j<m<=t} g_m = exp(G_t - G_j) on and below the diagonal,
+    // zeros above it (the blocked inverse relies on them); Gamma_t = exp(G_t)
+    for (int idx = tid; idx < kCh * kCh; idx += kThreads) {
+      const int t = idx / kCh, j = idx % kCh;
+      sD[t * kAS + j] = (j <= t) ? expf(sG[t] - sG[j]) : 0.f;
+    }
+    if (tid < kCh) sGam[tid] = expf(sG[tid]);
     __syncthreads();
     // per v-head operands: W hi, W lo, MQ hi, MQ lo, each [t][j] (K = 64), zero above the diagonal
     uint8_t* wq = reinterpret_cast<uint8_t*>(p.ws.wm) + (size_t(c) * p.Hv + h) * (4 * kCh * kCh * 2);
@@ -314,48 +324,72 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       gd[kCh + tid] = sD[(kCh - 1) * kAS + tid];
     }
     __syncthreads();
-    // X = (I + L)^-1, blocked: the four 16 x 16 diagonal blocks by forward substitution
-    // (column j by four lanes, m split mod 4; each lane reads back only the X entries it wrote),
-    // then X21 = -X22 L21 X11 for the 16 x 16 and then the 32 x 32 off-diagonal blocks.  X
-    // overwrites D.
-    {
-      const int j = tid >> 2, part = tid & 3;
-      const int jb = j & ~15;  // first row / column of j's diagonal block
-      const unsigned mask = 0xFu << (threadIdx.x & 28);
-      if (part == 0) sD[j * kAS + j] = 1.f;
-      for (int t = j + 1; t < jb + 16; ++t) {
-        float s = 0.f;
-        for (int m = j + part; m < t; m += 4) s = fmaf(sL[t * kAS + m], sD[m * kAS + j], s);
-        s += __shfl_xor_sync(mask, s, 1);
-        s += __shfl_xor_sync(mask, s, 2);
-        if (part == ((t - j) & 3)) sD[t * kAS + j] = -s;
+    // X = (I + L)^-1, blocked.  The four 16 x 16 diagonal blocks: one thread per column, forward
+    // substitution unrolled in registers (x_t = 0 above the diagonal, 1 on it).  Then
+    // X21 = -X22 (L21 X11) for the 16 x 16 and the 32 x 32 off-diagonal blocks, whose upper
+    // triangles are zero.  X overwrites D.
+    if (tid < kCh) {
+      const int jb = tid & ~15, jj = tid & 15;
+      float x[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) {
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < t; ++m) acc = fmaf(sL[(jb + t) * kAS + jb + m], x[m], acc);
+        x[t] = (t < jj) ? 0.f : ((t == jj) ? 1.f : -acc);
       }
+#pragma unroll
+      for (int t = 0; t < 16; ++t) sD[(jb + t) * kAS + tid] = x[t];
     }
     __syncthreads();
     float* sY2 = sm + L::OFF_Y2;
-#pragma unroll 1
-    for (int bs = 16; bs < kCh; bs *= 2) {
-      // blocks of size 2 bs at offsets o = 0, 2 bs, ...: Y = L21 X11, then X21 = -X22 Y
-      const int nblk = kCh / (2 * bs);
-      const int per = bs * bs;  // Y entries of one block
-      for (int idx = tid; idx < nblk * per; idx += kThreads) {
-        const int blk = idx / per, ii = (idx % per) / bs, jj = idx % bs;
-        const int o = 2 * bs * blk;
-        float y = 0.f;
-        for (int k = jj; k < bs; ++k) y = fmaf(sL[(o + bs + ii) * kAS + o + k], sD[(o + k) * kAS + o + jj], y);
-        sY2[(blk * bs + ii) * 33 + jj] = y;
+    {  // 16 x 16 off-diagonal blocks of the two 32 x 32 blocks: thread = (block, row, 2 columns)
+      const int blk = tid >> 7, ii = (tid >> 3) & 15, jj = 2 * (tid & 7);
+      const int o = 32 * blk;
+      float y0 = 0.f, y1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float l = sL[(o + 16 + ii) * kAS + o + k];
+        y0 = fmaf(l, sD[(o + k) * kAS + o + jj], y0);
+        y1 = fmaf(l, sD[(o + k) * kAS + o + jj + 1], y1);
       }
+      sY2[(16 * blk + ii) * 33 + jj] = y0;
+      sY2[(16 * blk + ii) * 33 + jj + 1] = y1;
       __syncthreads();
-      for (int idx = tid; idx < nblk * per; idx += kThreads) {
-        const int blk = idx / per, ii = (idx % per) / bs, jj = idx % bs;
-        const int o = 2 * bs * blk;
-        float x = 0.f;
-        for (int k = 0; k <= ii; ++k) x = fmaf(sD[(o + bs + ii) * kAS + o + bs + k], sY2[(blk * bs + k) * 33 + jj], x);
-        sD[(o + bs + ii) * kAS + o + jj] = -x;
+      float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float xv = sD[(o + 16 + ii) * kAS + o + 16 + k];
+        x0 = fmaf(xv, sY2[(16 * blk + k) * 33 + jj], x0);
+        x1 = fmaf(xv, sY2[(16 * blk + k) * 33 + jj + 1], x1);
       }
-      __syncthreads();
+      sD[(o + 16 + ii) * kAS + o + jj] = -x0;
+      sD[(o + 16 + ii) * kAS + o + jj + 1] = -x1;
     }
-    // W = X diag(beta) on and below the diagonal
+    __syncthreads();
+    {  // the 32 x 32 off-diagonal block: thread = (row, 4 columns)
+      const int ii = tid >> 3, jj = 4 * (tid & 7);
+      float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float l = sL[(32 + ii) * kAS + k];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) y[q] = fmaf(l, sD[k * kAS + jj + q], y[q]);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sY2[ii * 33 + jj + q] = y[q];
+      __syncthreads();
+      float x[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float xv = sD[(32 + ii) * kAS + 32 + k];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) x[q] = fmaf(xv, sY2[k * 33 + jj + q], x[q]);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) sD[(32 + ii) * kAS + jj + q] = -x[q];
+    }
+    __syncthreads();
     for (int idx = tid; idx < kCh * (kCh / 8); idx += kThreads) {
       const int cm = idx >> 3, r8 = idx & 7;
       const int t = (cm >> 3) * 8 + r8, jb = cm & 7;
@@ -866,7 +900,7 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
 size_t prefill_workspace_bytes(int B, long long N, int Hk, int Hv, int dk) {
   const long long cap = prefill_chunk_cap(B, N);
   const size_t meta = ((size_t(B) + 5 + 3) & ~size_t(3)) * 4;
-  return meta + size_t(cap) * (size_t(Hk) * kKqBlocks * kCh * dk * 2 + size_t(Hv) * (4 * kCh * kCh * 2 + 2 * kCh * 4));
+  return meta + size_t(cap) * (16 + size_t(Hk) * kKqBlocks * kCh * dk * 2 + size_t(Hv) * (4 * kCh * kCh * 2 + 2 * kCh * 4));
 }
 
 PrefillWorkspace prefill_workspace_carve(void* base, int B, long long N, int Hk, int Hv, int dk) {
@@ -875,6 +909,8 @@ PrefillWorkspace prefill_workspace_carve(void* base, int B, long long N, int Hk,
   char* p = static_cast<char*>(base);
   w.meta = reinterpret_cast<int32_t*>(p);
   p += ((size_t(B) + 5 + 3) & ~size_t(3)) * 4;
+  w.chunks = reinterpret_cast<int4*>(p);
+  p += size_t(w.chunk_cap) * 16;
   w.kq = reinterpret_cast<uint16_t*>(p);
   p += size_t(w.chunk_cap) * Hk * kKqBlocks * kCh * dk * 2;
   w.wm = reinterpret_cast<uint16_t*>(p);
