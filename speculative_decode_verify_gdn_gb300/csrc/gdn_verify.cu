@@ -103,8 +103,13 @@ struct TreeTable {
 };
 
 __device__ __forceinline__ void build_tree(const VerifyParams& p, int b, TreeTable* tt, bool report) {
-  for (int t = 0; t < p.K; ++t) {
-    int par = p.parent[size_t(b) * p.K + t];
+  int pr[kKMax];  // every parent index in flight at once, before the table is written
+#pragma unroll
+  for (int t = 0; t < kKMax; ++t) pr[t] = (t < p.K) ? p.parent[size_t(b) * p.K + t] : -1;
+#pragma unroll
+  for (int t = 0; t < kKMax; ++t) {
+    if (t >= p.K) break;
+    int par = pr[t];
     if (par < -1 || par >= t) {
       if (report) atomicOr(p.err, kDevErrTreeParent);
       par = -1;
@@ -493,10 +498,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
-    if constexpr (kTree) build_tree(p, b, tree, false);
   }
   if constexpr (kGated) cluster_arrive_relaxed();  // this CTA runs: the head's peers may write its smem later
-  __syncthreads();  // the barrier (and the tree table) are ready before any thread uses them
+  __syncthreads();  // the barrier is ready before any thread uses it
   // gated: this thread's two z values of the epilogue, (token tid/32, row tid%32) and eight
   // tokens later, fetched now so that they have long arrived when the epilogue runs
   uint32_t zz = 0;
@@ -520,6 +524,12 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
     else if (Lp > 0 && Lp < K)
       s0 = p.state_inter_prev + (size_t(b) * (K - 1) + (Lp - 1)) * size_t(p.Hv) * DV * DK + (size_t(h) * DV + r0) * DK;
     bulk_load(sS0, s0, L::S0_BYTES, bar);
+  }
+  if constexpr (kTree) {  // (off thread 0, and before it waits for the prologue grid)
+    if (tid == 32) build_tree(p, b, tree, false);
+    __syncthreads();  // the tree table is ready before the conv reads it
+  }
+  if (tid == 0) {
     griddep_wait();  // the prologue grid has finished and its tables are visible
     const size_t head = size_t(b) * p.Hk + kh;
     bulk_load(sWT, p.ws.wt + head * DK * kNCol, L::WT_BYTES, bar);
@@ -682,14 +692,35 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   float* inter = p.state_inter ? p.state_inter + size_t(b) * (K - 1) * inter_stride + head_tile_off + my_off : nullptr;
   for (int t = 0; t < K; ++t) {
     if constexpr (kTree) {
-      // a node that does not continue the previous one starts from its parent's state: S0 (still
-      // in shared memory) or the parent's intermediate, which this same lane stored earlier
+      // a node that does not continue the previous one starts from its parent's state, rebuilt
+      // from shared memory in its closed form S_par = Gamma_par S0 + sum_{j in path(par)}
+      // D[par][j] u_j k^_j^T (D: the product of g over the path nodes after j), walking the path
+      // upwards; no reload of the parent's intermediate from global memory
       const int par = tree->parent[t];
       if (t > 0 && par != t - 1) {
 #pragma unroll
-        for (int q = 0; q < F4; ++q)
-          s[q] = (par < 0) ? *reinterpret_cast<const float4*>(sS0 + (row0 + rowq[q]) * DK + 4 * c4)
-                           : *reinterpret_cast<const float4*>(inter + size_t(par) * inter_stride + size_t(rowq[q]) * DK);
+        for (int q = 0; q < F4; ++q) s[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        float d = 1.f;
+        for (int j = par; j >= 0; j = tree->parent[j]) {
+          const float4 kj = *reinterpret_cast<const float4*>(sKn + j * DK + 4 * c4);
+#pragma unroll
+          for (int q = 0; q < F4; ++q) {
+            const float uj = d * sU[j * kRowsPerWarp + rowq[q]];
+            s[q].x = fmaf(uj, kj.x, s[q].x);
+            s[q].y = fmaf(uj, kj.y, s[q].y);
+            s[q].z = fmaf(uj, kj.z, s[q].z);
+            s[q].w = fmaf(uj, kj.w, s[q].w);
+          }
+          d *= gG[j];
+        }
+#pragma unroll
+        for (int q = 0; q < F4; ++q) {
+          const float4 s0v = *reinterpret_cast<const float4*>(sS0 + (row0 + rowq[q]) * DK + 4 * c4);
+          s[q].x = fmaf(d, s0v.x, s[q].x);
+          s[q].y = fmaf(d, s0v.y, s[q].y);
+          s[q].z = fmaf(d, s0v.z, s[q].z);
+          s[q].w = fmaf(d, s0v.w, s[q].w);
+        }
       }
     }
     const float g = gG[t];
