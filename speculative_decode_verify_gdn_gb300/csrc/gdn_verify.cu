@@ -131,16 +131,19 @@ __device__ __forceinline__ void build_tree(const VerifyParams& p, int b, TreeTab
 
 // Conv + SiLU of one channel over the window (a chain of K tokens, or a token tree when kTree);
 // writes the channel's K history snapshots and its new history (that after token / node K-1).
-// y[t] receives the outputs for t < K.
-template <bool kTree>
+// y[t] receives the outputs for t < K.  A token tree reads each node's window through the
+// table's indices, from `scratch` (3 + kKMax floats of shared memory) when given, else from a
+// thread-local array.
+template <bool kTree, bool kScratch = false>
 __device__ __forceinline__ void conv_channel(const VerifyParams& p, int b, int c, const TreeTable* tt,
-                                             float (&y)[kKMax]) {
+                                             float (&y)[kKMax], float* scratch = nullptr) {
   if constexpr (kTree) {
     const int C = p.C;
     const int K = p.K;
     const float4 w = *reinterpret_cast<const float4*>(p.conv_w + size_t(c) * kConvW);
     const float* hin = p.conv_state_in + size_t(b) * 3 * C + c;
-    float vals[3 + kKMax];  // [history rows 0..2, x_0 .. x_{K-1}]
+    float local_vals[kScratch ? 1 : 3 + kKMax];
+    float* vals = kScratch ? scratch : local_vals;  // [history rows 0..2, x_0 .. x_{K-1}]
     vals[0] = hin[0];
     vals[1] = hin[C];
     vals[2] = hin[2 * C];
@@ -541,7 +544,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   if (lane >= 4 && lane < 4 + kRowsPerWarp) {
     const int i = warp * kRowsPerWarp + (lane - 4);
     float y[kKMax];
-    conv_channel<kTree>(p, b, 2 * p.Hk * DK + h * DV + r0 + i, tree, y);
+    // (a token tree's window values go through this row of the P table, which the warp only
+    // fills after the load wait)
+    conv_channel<kTree, true>(p, b, 2 * p.Hk * DK + h * DV + r0 + i, tree, y, sm + L::OFF_P + i * L::PSTRIDE);
 #pragma unroll
     for (int t = 0; t < kKMax; ++t) sV[t * kRowsPerWarp + (lane - 4)] = y[t];
   }
