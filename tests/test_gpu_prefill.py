@@ -161,3 +161,12 @@ def test_serving_shape_prompts_against_oracle():
     d, lay, pr = _problem(1208, [1000, 333, 64, 0], Hk=dims.Hk, Hv=dims.Hv, dk=dims.dk, dv=dims.dv,
                           dists=WORKLOADS["serve16"].dists)
     _check(_run(d, lay, pr, out_f32=False), _oracle(d, lay, pr), OUT_TOL_BF16)
+
+
+def test_many_short_prompts():
+    """1500 prompts of 0..5 tokens: the offset check and chunk numbering take several prompts per
+    thread, most prompts are shorter than the conv history, and many are empty."""
+    g0 = Gen(1209)
+    lens = [int(v) for v in g0.integers((1500,), 0, 5)]
+    d, lay, pr = _problem(1210, lens, Hk=1, Hv=2, dk=64, dv=64)
+    _check(_run(d, lay, pr), _oracle(d, lay, pr))
