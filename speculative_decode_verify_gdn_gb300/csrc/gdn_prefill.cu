@@ -418,8 +418,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
 //   u  = r W^T           (r = v - Gamma o P_k, written by the threads)
 //   o' = u MQ^T          (out = q_scale (Gamma o P_q + o'))
 //   S  = Gamma_63 S + (d o u) k^   (accumulated into the TMEM state, B = k^T hi/lo)
-// Thread roles: one thread issues the MMAs; in the epilogues lanes 0..15 of warp w hold state
-// row 16 (w % 4) + lane, warps w and w + 4 splitting the columns.
+// Thread roles: warps 0..7 run the epilogues (lanes 0..15 of warp w hold state row
+// 16 (w % 4) + lane, warps w and w + 4 splitting the columns); a ninth warp's first thread issues
+// the bulk copies and the MMAs, so that its stalls on the MMA queue delay no epilogue.
 template <int DK>
 struct TcLayout {
   static constexpr int BLK_KQ = kCh * DK * 2;            // one 64 x DK bf16 operand
@@ -452,8 +453,28 @@ __device__ __forceinline__ bool wait_failed(uint64_t* bar, uint32_t parity) {
   return __syncthreads_or(!ok) != 0;
 }
 
+// One product of the chunk form as three bf16 MMA chains over hi/lo operand pairs (hi.hi, hi.lo,
+// lo.hi) of KSTEPS steps of K = 16 each.  Descriptors are formed once; a K step moves the start
+// address field by 256 bytes (two core matrices).
+template <int KSTEPS>
+__device__ __forceinline__ void umma_split3(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
+                                            uint32_t sbo, uint32_t idesc, bool accumulate) {
+  const uint64_t dah = umma_smem_desc(a_hi, 128, sbo), dal = umma_smem_desc(a_lo, 128, sbo);
+  const uint64_t dbh = umma_smem_desc(b_hi, 128, sbo), dbl = umma_smem_desc(b_lo, 128, sbo);
+#pragma unroll
+  for (int sp = 0; sp < 3; ++sp) {
+    const uint64_t da = (sp == 2) ? dal : dah;
+    const uint64_t db = (sp == 1) ? dbl : dbh;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk)
+      umma_bf16(d, da + uint64_t(16 * kk), db + uint64_t(16 * kk), idesc, (accumulate || sp > 0 || kk > 0) ? 1u : 0u);
+  }
+}
+
+constexpr int kIssuer = kThreads;  // the state kernel's copy / MMA issuing thread (first of warp 8)
+
 template <int DK, int DV>
-__global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const PrefillParams p) {
+__global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(const PrefillParams p) {
   using L = TcLayout<DK>;
   extern __shared__ __align__(128) uint8_t smb[];
   constexpr int kHalves = DV / kTileRows;
@@ -477,7 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
   // epilogue coordinates: row m of the tile (lanes 0..15), column half hh
   const int quad = warp & 3, hh = warp >> 2;
   const int m = 16 * quad + (lane & 15);
-  const bool act = lane < 16;
+  const bool epi = warp < kThreads / 32;  // an epilogue warp (not the issuing warp)
+  const bool act = epi && lane < 16;
   const uint32_t lane_sel = uint32_t(32 * quad) << 16;
 
   if (tid == 0) {
@@ -525,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     bulk_load(smb + L::OFF_GD + b * 2 * kCh * 4, p.ws.gd + (size_t(c) * p.Hv + h) * (2 * kCh), 2 * kCh * 4,
               bar + kBarGD0 + b);
   };
-  if (tid == 0 && n_chunks > 0) {
+  if (tid == kIssuer && n_chunks > 0) {
     issue_kq(c_first);
     issue_kt(c_first);
     issue_w(c_first);
@@ -550,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
   {
     const float* src = p.state_in + ((size_t(i) * p.Hv + h) * DV + r0 + m) * DK + hh * SC;
 #pragma unroll
-    for (int c0 = 0; c0 < SC; c0 += 16) {
+    for (int c0 = 0; c0 < SC && epi; c0 += 16) {
       float v[16];
 #pragma unroll
       for (int q = 0; q < 16; q += 4) {
@@ -600,7 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
       failed = true;
     } else {
       tc_fence_after();
-      scale_state(reinterpret_cast<const float*>(smb + L::OFF_GD));
+      if (epi) scale_state(reinterpret_cast<const float*>(smb + L::OFF_GD));
       tc_fence_before();
       __syncthreads();
       tc_fence_after();
@@ -615,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     len = int(min_ll(kCh, s1 - tok0));
 
     // (a) raw x of this chunk to rows 3..66; the next chunk's x is fetched meanwhile
-    {
+    if (tid < kThreads) {
       const uint32_t wv[8] = {xr0.x, xr0.y, xr0.z, xr0.w, xr1.x, xr1.y, xr1.z, xr1.w};
       float* row = sX + (xt + 3) * kTileRows + 16 * xg;
 #pragma unroll
@@ -634,20 +656,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     // (b) P = S [k^ | q^]^T on the tensor cores (k^ and q^ stacked as one N = 128 operand, the
     // result in the adjacent P_k | P_q columns), while the threads run the conv of their row m
     // (channel m) over their 32 tokens
-    if (tid == 0) {
+    if (tid == kIssuer) {
       if (mbar_wait_bounded(bar + kBarKQ, par)) {
         tc_fence_after();
         const uint32_t sS = sbase + L::OFF_S, sKQ = sbase + L::OFF_KQ;
-        constexpr uint32_t sbo = (DK / 8) * 128;
-#pragma unroll 1
-        for (int sp = 0; sp < 3; ++sp) {  // hi.hi, hi.lo, lo.hi
-          const uint32_t a = sS + (sp == 2 ? L::BLK_KQ : 0);
-          const uint32_t b = sKQ + (sp == 1 ? 2 * L::BLK_KQ : 0);
-#pragma unroll 1
-          for (int kk = 0; kk < DK / 16; ++kk)
-            umma_bf16(tmem + kColPk, umma_smem_desc(a + kk * 256, 128, sbo), umma_smem_desc(b + kk * 256, 128, sbo),
-                      id_n128, (sp | kk) != 0);
-        }
+        umma_split3<DK / 16>(tmem + kColPk, sS, sS + L::BLK_KQ, sKQ, sKQ + 2 * L::BLK_KQ, (DK / 8) * 128, id_n128,
+                             false);
         umma_commit(bar + kBarPk);
         ++armed[kBarPk];
       }
@@ -669,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     }
     tc_fence_after();
     // (c) r = v - Gamma o P_k -> operand
-    {
+    if (epi) {
       float pk[32];
       tmem_ld32(tmem + lane_sel + kColPk + 32 * hh, pk);
       if (act) {
@@ -677,27 +691,20 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
         for (int q = 0; q < 32; ++q) pk[q] = fmaf(-sGam[32 * hh + q], pk[q], v[q]);
         store_pair(L::OFF_RD, m, 32 * hh, kCh, pk, 32);
       }
-      // the last three raw rows become the next chunk's history (the conv is done with them)
-      if (len == kCh)
-        for (int idx = tid; idx < 3 * kTileRows; idx += kThreads) sX[idx] = sX[kCh * kTileRows + idx];
     }
+    // the last three raw rows become the next chunk's history (the conv is done with them)
+    if (len == kCh)
+      for (int idx = tid; idx < 3 * kTileRows; idx += kThreads + 32) sX[idx] = sX[kCh * kTileRows + idx];
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     // (d) u = r W^T; once the q^ MMAs are done too, the next chunk's k^|q^ may come in
-    if (tid == 0) {
+    if (tid == kIssuer) {
       if (mbar_wait_bounded(bar + kBarW, par)) {
         tc_fence_after();
-#pragma unroll 1
-        for (int sp = 0; sp < 3; ++sp) {
-          const uint32_t a = sbase + L::OFF_RD + (sp == 2 ? L::BLK : 0);
-          const uint32_t b = sbase + L::OFF_W + (sp == 1 ? L::BLK : 0);
-#pragma unroll 1
-          for (int kk = 0; kk < kCh / 16; ++kk)
-            umma_bf16(tmem + kColU, umma_smem_desc(a + kk * 256, 128, 1024), umma_smem_desc(b + kk * 256, 128, 1024),
-                      id_n64, (sp | kk) != 0);
-        }
+        umma_split3<kCh / 16>(tmem + kColU, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK, sbase + L::OFF_W,
+                              sbase + L::OFF_W + L::BLK, 1024, id_n64, false);
         umma_commit(bar + kBarU);
         ++armed[kBarU];
       }
@@ -708,7 +715,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
       break;
     }
     tc_fence_after();
-    {
+    if (epi) {
       float u[32];
       tmem_ld32(tmem + lane_sel + kColU + 32 * hh, u);
       if (act) {
@@ -723,32 +730,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     __syncthreads();
     tc_fence_after();
     // (e) o' = u MQ^T (own commit), then S += (d o u) k^
-    if (tid == 0) {
+    if (tid == kIssuer) {
       if (lc + 1 < n_chunks) issue_w(c_first + lc + 1);
       if (mbar_wait_bounded(bar + kBarMQ, par)) {
         tc_fence_after();
-#pragma unroll 1
-        for (int sp = 0; sp < 3; ++sp) {
-          const uint32_t a = sbase + L::OFF_U + (sp == 2 ? L::BLK : 0);
-          const uint32_t b = sbase + L::OFF_MQ + (sp == 1 ? L::BLK : 0);
-#pragma unroll 1
-          for (int kk = 0; kk < kCh / 16; ++kk)
-            umma_bf16(tmem + kColO, umma_smem_desc(a + kk * 256, 128, 1024), umma_smem_desc(b + kk * 256, 128, 1024),
-                      id_n64, (sp | kk) != 0);
-        }
+        umma_split3<kCh / 16>(tmem + kColO, sbase + L::OFF_U, sbase + L::OFF_U + L::BLK, sbase + L::OFF_MQ,
+                              sbase + L::OFF_MQ + L::BLK, 1024, id_n64, false);
         umma_commit(bar + kBarO);
         ++armed[kBarO];
       }
       if (mbar_wait_bounded(bar + kBarKT, par)) {
-#pragma unroll 1
-        for (int sp = 0; sp < 3; ++sp) {
-          const uint32_t a = sbase + L::OFF_RD + (sp == 2 ? L::BLK : 0);
-          const uint32_t b = sbase + L::OFF_KT + (sp == 1 ? L::BLK_KQ : 0);
-#pragma unroll 1
-          for (int kk = 0; kk < kCh / 16; ++kk)
-            umma_bf16(tmem + kColS, umma_smem_desc(a + kk * 256, 128, 1024), umma_smem_desc(b + kk * 256, 128, 1024),
-                      id_ndk, 1u);
-        }
+        umma_split3<kCh / 16>(tmem + kColS, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK, sbase + L::OFF_KT,
+                              sbase + L::OFF_KT + L::BLK_KQ, 1024, id_ndk, true);
         umma_commit(bar + kBarS);
         ++armed[kBarS];
       }
@@ -764,7 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     // outputs, while the state update runs: staged token-major in the u operand buffer (the o'
     // MMAs are done with it) and written out after the next barrier as 16-byte stores
     float* sOut = reinterpret_cast<float*>(smb + L::OFF_U);  // [64 tokens][64 rows]
-    {
+    if (epi) {
       float o[32], pq[32];
       tmem_ld32(tmem + lane_sel + kColO + 32 * hh, o);
       tmem_ld32(tmem + lane_sel + kColPq + 32 * hh, pq);
@@ -785,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
       }
     }
     tc_fence_after();
-    if (xt < len) {  // thread = (token xt, rows 16 xg .. 16 xg + 15)
+    if (tid < kThreads && xt < len) {  // thread = (token xt, rows 16 xg .. 16 xg + 15)
       const float* src = sOut + xt * kTileRows + 16 * xg;
       const size_t oi = size_t(tok0 + xt) * p.Hv * DV + size_t(h) * DV + r0 + 16 * xg;
       if (p.out_f32) {
@@ -804,7 +797,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
         o4[1] = make_uint4(w[4], w[5], w[6], w[7]);
       }
     }
-    {
+    if (epi) {
       const float gl = more ? reinterpret_cast<const float*>(smb + L::OFF_GD + ((lc + 1) & 1) * 2 * kCh * 4)[kCh - 1] : 1.f;
 #pragma unroll
       for (int c0 = 0; c0 < SC; c0 += 32) {
@@ -822,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (tid == 0 && more) {
+    if (tid == kIssuer && more) {
       issue_mq(c_first + lc + 1);
       issue_kt(c_first + lc + 1);
       if (lc + 2 < n_chunks) issue_gd(lc + 2);
@@ -830,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
   }
 
   if (failed) {
-    if (tid == 0) {  // one more bounded wait for every copy and MMA group still in flight
+    if (tid == kIssuer) {  // one more bounded wait for every copy and MMA group still in flight
       atomicOr(p.err, kDevErrTimeout);
       for (int q = 0; q < L::NBAR; ++q)
         if (armed[q] > 0) (void)mbar_wait_bounded(bar + q, uint32_t(armed[q] - 1) & 1u);
@@ -839,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prefill_state_kernel(const Pr
     // final state from TMEM
     float* dst = p.state_out + ((size_t(i) * p.Hv + h) * DV + r0 + m) * DK + hh * SC;
 #pragma unroll
-    for (int c0 = 0; c0 < SC; c0 += 32) {
+    for (int c0 = 0; c0 < SC && epi; c0 += 32) {
       float sv[32];
       tmem_ld32(tmem + lane_sel + kColS + hh * SC + c0, sv);
       if (act)
@@ -891,7 +884,7 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   k1<<<dim3(unsigned(p.ws.chunk_cap), unsigned(p.Hk), 1), kThreads, b1, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k2<<<dim3(unsigned(p.Hv * (DV / kTileRows)), unsigned(p.B), 1), kThreads, b2, stream>>>(p);
+  k2<<<dim3(unsigned(p.Hv * (DV / kTileRows)), unsigned(p.B), 1), kThreads + 32, b2, stream>>>(p);
   return cudaGetLastError();
 }
 
