@@ -131,31 +131,58 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
     sAB[(2 * e + 1) * kCh + t] = (t < len) ? bf16_to_f32(p.b[gi]) : 0.f;
   }
 
-  // a1 for the head's 2 DK q|k channels, one thread per channel walking the chunk; the three
-  // rows before the chunk come from the prompt itself or, at its start, from the history
+  // a1 for the head's 2 DK q|k channels.  The raw x tile [64 tokens][2 DK] (q channels, then k)
+  // comes in with 16-byte loads, staged in the space of the conv table; then one thread per
+  // channel reads its column into registers and walks the chunk.  The three rows before the
+  // chunk come from the prompt itself or, at its start, from the history.
   float* sY = sm + L::OFF_Y;
-  for (int ch = tid; ch < 2 * DK; ch += kThreads) {
-    const size_t gch = (ch < DK) ? size_t(kh) * DK + ch : size_t(p.Hk) * DK + size_t(kh) * DK + (ch - DK);
-    const float4 w = *reinterpret_cast<const float4*>(p.conv_w + gch * kConvW);
-    float h[3];
-#pragma unroll
-    for (int m = 0; m < 3; ++m) {
-      const long long pos = tok0 - 3 + m;
-      h[m] = (pos >= s0) ? bf16_to_f32(p.x[size_t(pos) * C + gch])
-                         : p.conv_state_in[(size_t(i) * 3 + size_t(pos - s0 + 3)) * C + gch];
+  {
+    uint16_t* sXr = reinterpret_cast<uint16_t*>(sY);
+    constexpr int V8 = 2 * DK / 8;  // 16-byte groups per token row
+    for (int idx = tid; idx < kCh * V8; idx += kThreads) {
+      const int t = idx / V8, ch0 = 8 * (idx % V8);
+      const size_t gch0 = (ch0 < DK) ? size_t(kh) * DK + ch0 : size_t(p.Hk) * DK + size_t(kh) * DK + (ch0 - DK);
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t < len) v = *reinterpret_cast<const uint4*>(p.x + size_t(tok0 + t) * C + gch0);
+      *reinterpret_cast<uint4*>(sXr + t * 2 * DK + ch0) = v;
     }
-    uint16_t xs[kCh];  // all of the channel's loads in flight at once
+  }
+  __syncthreads();
+  static_assert(2 * DK <= kThreads, "one thread per q|k channel");
+  {
+    const int ch = tid;  // (threads beyond the 2 DK channels only join the barriers)
+    const bool own = ch < 2 * DK;
+    const size_t gch = (ch < DK) ? size_t(kh) * DK + ch : size_t(p.Hk) * DK + size_t(kh) * DK + (ch - DK);
+    float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+    float h0 = 0.f, h1 = 0.f, h2 = 0.f;
+    uint16_t xs[kCh];
+    if (own) {
+      w = *reinterpret_cast<const float4*>(p.conv_w + gch * kConvW);
+      float h[3];
 #pragma unroll
-    for (int t = 0; t < kCh; ++t) xs[t] = (t < len) ? p.x[size_t(tok0 + t) * C + gch] : uint16_t(0);
-    float h0 = h[0], h1 = h[1], h2 = h[2];
+      for (int m = 0; m < 3; ++m) {
+        const long long pos = tok0 - 3 + m;
+        h[m] = (pos >= s0) ? bf16_to_f32(p.x[size_t(pos) * C + gch])
+                           : p.conv_state_in[(size_t(i) * 3 + size_t(pos - s0 + 3)) * C + gch];
+      }
+      h0 = h[0];
+      h1 = h[1];
+      h2 = h[2];
+      const uint16_t* sXr = reinterpret_cast<const uint16_t*>(sY);
 #pragma unroll
-    for (int t = 0; t < kCh; ++t) {
-      const float xv = bf16_to_f32(xs[t]);
-      const float z = fmaf(w.w, xv, fmaf(w.z, h2, fmaf(w.y, h1, w.x * h0)));
-      sY[t * L::YS + ch] = (t < len) ? silu(z) : 0.f;
-      h0 = h1;
-      h1 = h2;
-      h2 = xv;
+      for (int t = 0; t < kCh; ++t) xs[t] = sXr[t * 2 * DK + ch];
+    }
+    __syncthreads();  // every column is read before the conv outputs overwrite the staging
+    if (own) {
+#pragma unroll
+      for (int t = 0; t < kCh; ++t) {
+        const float xv = bf16_to_f32(xs[t]);
+        const float z = fmaf(w.w, xv, fmaf(w.z, h2, fmaf(w.y, h1, w.x * h0)));
+        sY[t * L::YS + ch] = (t < len) ? silu(z) : 0.f;
+        h0 = h1;
+        h1 = h2;
+        h2 = xv;
+      }
     }
   }
   __syncthreads();
