@@ -170,19 +170,6 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 // Generic-proxy shared-memory writes become visible to the tensor core (async proxy).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-// 16 consecutive 32-bit columns of this thread's TMEM lane (warp w reads lanes 32 (w % 4) ..).
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(r[q]);
-}
-
 // 32 consecutive 32-bit columns of this thread's TMEM lane, one load and one wait.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
@@ -228,15 +215,9 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// x = hi + lo with hi = bf16(x), lo = bf16(x - hi): the pair carries 16 significant bits, so
-// hi.hi + hi.lo + lo.hi reproduces an f32 product to about 2^-16.
-__device__ __forceinline__ void split_bf16(float x, uint16_t& hi, uint16_t& lo) {
-  hi = f32_to_bf16(x);
-  lo = f32_to_bf16(x - bf16_to_f32(hi));
-}
-
-// Eight f32 values -> their bf16 hi and lo parts (as split_bf16), packed as two 16-byte words,
-// element 2q in the low half of word q; paired hardware conversions (cvt.rn.bf16x2.f32).
+// Eight f32 values x -> their bf16 parts hi = bf16(x), lo = bf16(x - hi), packed as two 16-byte
+// words, element 2q in the low half of word q (paired hardware conversions).  The pair carries
+// 16 significant bits, so hi.hi + hi.lo + lo.hi reproduces an f32 product to about 2^-16.
 __device__ __forceinline__ void split8(const float* v, uint4& hi, uint4& lo) {
   uint32_t h[4], l[4];
 #pragma unroll

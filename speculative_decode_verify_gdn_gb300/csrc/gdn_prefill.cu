@@ -463,7 +463,7 @@ struct TcLayout {
   static constexpr int OFF_X = OFF_U + 2 * BLK;          // raw x [67][64] f32 (3 history rows)
   static constexpr int OFF_TAP = OFF_X + 67 * kTileRows * 4;  // conv taps [64][4]
   static constexpr int OFF_BAR = OFF_TAP + kTileRows * 16;    // mbarriers
-  static constexpr int NBAR = 11;
+  static constexpr int NBAR = 10;
   static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_TSLOT + 16;
   static_assert(OFF_TAP % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
@@ -472,7 +472,7 @@ struct TcLayout {
 // TMEM columns
 constexpr uint32_t kColS = 0, kColPk = 128, kColPq = 192, kColU = 256, kColO = 320, kTmemCols = 512;
 // mbarriers
-enum { kBarKQ = 0, kBarKT, kBarW, kBarMQ, kBarGD0, kBarGD1, kBarPk, kBarPq, kBarU, kBarO, kBarS };
+enum { kBarKQ = 0, kBarKT, kBarW, kBarMQ, kBarGD0, kBarGD1, kBarPk, kBarU, kBarO, kBarS };
 
 // every thread waits (bounded); true when any thread of the CTA gave up
 __device__ __forceinline__ bool wait_failed(uint64_t* bar, uint32_t parity) {
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
   const uint32_t tmem = *tslot;
 
   // phases armed per barrier (thread 0 only), so that a failed CTA can wait for what it started
-  int armed[L::NBAR] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+  int armed[L::NBAR] = {};
   auto issue_kq = [&](int c) {
     ++armed[kBarKQ];
     mbar_arrive_expect_tx(bar + kBarKQ, 4 * L::BLK_KQ);

@@ -467,7 +467,7 @@ struct StreamLayout {
   static constexpr uint32_t GATE_BYTES = kGateFloats * 4;
   static constexpr uint32_t KN_BYTES = kKMax * DK * 4;
   static constexpr uint32_t kRowsBytesW = kRows * 4;
-  static_assert(OFF_NW % 4 == 0, "gated-norm bulk destination 16-byte aligned");
+  static_assert(OFF_NW % 4 == 0 && kRowsBytesW % 16 == 0, "gated-norm bulk copy 16-byte aligned");
   static_assert(S0_BYTES % 16 == 0 && WT_BYTES % 16 == 0 && GATE_BYTES % 16 == 0 && KN_BYTES % 16 == 0, "");
   static_assert(OFF_WT % 4 == 0 && OFF_GATE % 4 == 0 && OFF_KN % 4 == 0 && OFF_P % 4 == 0,
                 "bulk destinations and float4 rows 16-byte aligned");
