@@ -456,18 +456,16 @@ struct StreamLayout {
   static constexpr int OFF_R = OFF_P + kRows * PSTRIDE;                // [32][RSTRIDE] rhs, then o (gated)
   static constexpr int OFF_X = OFF_R + kRows * RSTRIDE;                // tree table or gated-norm block
   static constexpr int OFF_TREE = OFF_X;                                 // TreeTable (token trees only)
-  static constexpr int OFF_SQ = OFF_X;                                   // gated: sums of o^2 [tile][warp][16]
-  static constexpr int OFF_NW = OFF_SQ + 4 * kWarps * kKMax;             // gated: norm weight [32], bulk copy
-  static constexpr int X_FLOATS = kGated ? 4 * kWarps * kKMax + kRows : int(sizeof(TreeTable) / 4);
-  static constexpr int OFF_BAR = (OFF_X + X_FLOATS + 1) & ~1;            // 8-byte aligned mbarrier
-  static constexpr int FLOATS = OFF_BAR + 2;
+  static constexpr int OFF_SQ = OFF_X;  // gated: sums of o^2 [tile][warp][8] float2 (tokens c, c + 8)
+  static constexpr int X_FLOATS = kGated ? 4 * kWarps * kKMax : int(sizeof(TreeTable) / 4);
+  static constexpr int OFF_BAR = (OFF_X + X_FLOATS + 1) & ~1;            // 8-byte aligned mbarrier(s)
+  static constexpr int FLOATS = OFF_BAR + (kGated ? 4 : 2);              // gated: + the exchange mbarrier
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
   static constexpr uint32_t S0_BYTES = kRows * DK * 4;
   static constexpr uint32_t WT_BYTES = DK * kNCol * 4;
   static constexpr uint32_t GATE_BYTES = kGateFloats * 4;
   static constexpr uint32_t KN_BYTES = kKMax * DK * 4;
-  static constexpr uint32_t kRowsBytesW = kRows * 4;
-  static_assert(OFF_NW % 4 == 0 && kRowsBytesW % 16 == 0, "gated-norm bulk copy 16-byte aligned");
+  static_assert(OFF_SQ % 2 == 0, "gated exchange slots 8-byte aligned");
   static_assert(S0_BYTES % 16 == 0 && WT_BYTES % 16 == 0 && GATE_BYTES % 16 == 0 && KN_BYTES % 16 == 0, "");
   static_assert(OFF_WT % 4 == 0 && OFF_GATE % 4 == 0 && OFF_KN % 4 == 0 && OFF_P % 4 == 0,
                 "bulk destinations and float4 rows 16-byte aligned");
@@ -498,26 +496,22 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   float* sU = sm + L::OFF_U + warp * kKMax * kRowsPerWarp;
 
   TreeTable* tree = reinterpret_cast<TreeTable*>(sm + L::OFF_TREE);
+  // gated: the partial sums of o^2 of all kTiles CTAs of the head land on bar_sq (8 bytes from
+  // each of 8 lanes of every warp of every CTA, own included)
+  uint64_t* bar_sq = bar + 1;
+  constexpr uint32_t kSqBytes = uint32_t(kTiles * kWarps * 8 * 8);
   if (tid == 0) {
     mbar_init(bar, 1);
+    if constexpr (kGated) {
+      mbar_init(bar_sq, 1);
+      mbar_arrive_expect_tx(bar_sq, kSqBytes);
+    }
     fence_mbar_init();
   }
   if constexpr (kGated) cluster_arrive_relaxed();  // this CTA runs: the head's peers may write its smem later
   __syncthreads();  // the barrier is ready before any thread uses it
-  // gated: this thread's two z values of the epilogue, (token tid/32, row tid%32) and eight
-  // tokens later, fetched now so that they have long arrived when the epilogue runs
-  uint32_t zz = 0;
-  if constexpr (kGated) {
-    const int t0 = tid / kRows, i0 = tid % kRows;
-    const uint16_t* zp = p.z + ((size_t(b) * K + t0) * p.Hv + h) * DV + r0 + i0;
-    if (t0 < K) zz = __ldg(zp);
-    if (t0 + 8 < K) zz |= uint32_t(__ldg(zp + size_t(8) * p.Hv * DV)) << 16;
-  }
   if (tid == 0) {
-    uint32_t extra = 0;
-    if constexpr (kGated) extra = L::kRowsBytesW;
-    mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES + extra);
-    if constexpr (kGated) bulk_load(sm + L::OFF_NW, p.norm_w + r0, L::kRowsBytesW, bar);
+    mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES);
     // S0: the previous final state, or (rollback applied on read) the accepted intermediate or
     // the pre-window snapshot of the previous window
     const int Lp = prev_accept(p, b, blockIdx.x == 0);
@@ -527,6 +521,18 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
     else if (Lp > 0 && Lp < K)
       s0 = p.state_inter_prev + (size_t(b) * (K - 1) + (Lp - 1)) * size_t(p.Hv) * DV * DK + (size_t(h) * DV + r0) * DK;
     bulk_load(sS0, s0, L::S0_BYTES, bar);
+  }
+  // gated: the lane's two z values of the epilogue, (token cg, row m of its warp) and eight tokens
+  // later, and the row's norm weight, fetched now so that they have long arrived when used (the
+  // lane map (m, cg) is the one of the outputs phase below)
+  uint16_t z_a = 0, z_b = 0;
+  float nw = 0.f;
+  if constexpr (kGated) {
+    const int t0 = lane & 7, i0 = warp * kRowsPerWarp + (lane >> 3);
+    const uint16_t* zp = p.z + ((size_t(b) * K + t0) * p.Hv + h) * DV + r0 + i0;
+    if (t0 < K) z_a = __ldg(zp);
+    if (t0 + 8 < K) z_b = __ldg(zp + size_t(8) * p.Hv * DV);
+    nw = __ldg(p.norm_w + r0 + i0);
   }
   if constexpr (kTree) {  // (off thread 0, and before it waits for the prologue grid)
     if (tid == 32) build_tree(p, b, tree, false);
@@ -577,8 +583,8 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   const int m = lane >> 3;   // row of this warp handled by this lane in the phases below
   const int cg = lane & 7;   // column group (P) / token (outputs)
 
-  // (a gated CTA's warps take part in the cluster barriers below even after a timeout)
-  float sq_a = 0.f, sq_b = 0.f;  // gated: o^2 of tokens cg and cg + 8, summed over the warp's rows
+  // (a gated CTA's warps take part in the cluster exchange below even after a timeout)
+  float o_a = 0.f, o_b = 0.f;  // gated: o of (row m, tokens cg and cg + 8), normed at the end
   if (ok) {
   (void)mbar_try_wait(bar, 0);  // every lane observes the completed phase
 
@@ -638,11 +644,10 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
       float o = p.q_scale * gGam[t] * sP[(row0 + m) * L::PSTRIDE + kKMax + t];
       for (int jj = 0; jj <= t; ++jj) o = fmaf(gN[t * kMStride + jj], sU[jj * kRowsPerWarp + m], o);
       if constexpr (kGated) {
-        sR[(row0 + m) * L::RSTRIDE + t] = o;  // the rhs rows of this warp are dead after the substitution
         if (half == 0)
-          sq_a = o * o;
+          o_a = o;
         else
-          sq_b = o * o;
+          o_b = o;
       } else {
         const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
         if (p.out_f32)
@@ -655,24 +660,22 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   __syncwarp();
   }  // ok
 
-  const uint32_t rank = kGated ? cluster_ctarank() : 0;
   if constexpr (kGated) {
-    // sums of o^2 over the warp's 4 rows (lanes m = 0..3 of one column group), sent to every CTA
-    // of the cluster; nobody waits for them until the epilogue
+    // sums of o^2 over the warp's 4 rows (lanes m = 0..3 of one column group), pushed into every
+    // CTA of the cluster as asynchronous stores that complete on the receiver's bar_sq; the
+    // sender never waits for them, the receiver only in its epilogue
+    float sq_a = o_a * o_a, sq_b = o_b * o_b;
     sq_a += __shfl_xor_sync(0xffffffffu, sq_a, 8);
     sq_a += __shfl_xor_sync(0xffffffffu, sq_a, 16);
     sq_b += __shfl_xor_sync(0xffffffffu, sq_b, 8);
     sq_b += __shfl_xor_sync(0xffffffffu, sq_b, 16);
-    cluster_wait_acquire();  // every CTA of the cluster has started (pairs with the first arrive)
+    cluster_wait_acquire();  // every CTA of the cluster has started and set up bar_sq
     if (lane < 8) {
-      const uint32_t slot = smem_addr(sm + L::OFF_SQ + (rank * kWarps + warp) * kKMax + lane);
-      for (int d = 0; d < kTiles; ++d) {
-        const uint32_t a = map_to_rank(slot, d);
-        st_cluster_f32(a, sq_a);
-        st_cluster_f32(a + 8 * 4, sq_b);
-      }
+      const uint32_t rank = cluster_ctarank();
+      const uint32_t slot = smem_addr(sm + L::OFF_SQ + ((rank * kWarps + warp) * (kKMax / 2) + lane) * 2);
+      const uint32_t sbar = smem_addr(bar_sq);
+      for (int d = 0; d < kTiles; ++d) st_async_cluster_f32x2(map_to_rank(slot, d), sq_a, sq_b, map_to_rank(sbar, d));
     }
-    cluster_arrive_release();
   }
 
   if (ok) {
@@ -751,27 +754,37 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
 
   if constexpr (kGated) {
     // gated output norm over the head's dv rows, which the cluster's kTiles CTAs share:
-    // out = o rsqrt(sum_rows o^2 / dv + eps) w SiLU(z).  The wait pairs with every peer's arrive
-    // after its outputs phase, long past; it also orders this CTA's own o rows (written before its
-    // arrive) before the reads below, and no peer writes to this CTA's shared memory after it.
-    (void)rank;
-    cluster_wait_acquire();
-    const float* sO = sm + L::OFF_R;  // o of token t, row i at [i][t]
-    const float* sSq = sm + L::OFF_SQ;
+    // out = o rsqrt(sum_rows o^2 / dv + eps) w SiLU(z), per warp on the o values it holds.  Every
+    // CTA waits here for all pushes into its shared memory, so none exits while a peer still
+    // writes to it.
+    const bool got = mbar_wait_bounded(bar_sq, 0);
+    if (!got && lane == 0) atomicOr(p.err, kDevErrTimeout);
+    if (ok && got) {
+      // lane (m, cg) adds the partials of warps m, m + 4, ...; the xor over the m bits completes
+      const float2* sSq = reinterpret_cast<const float2*>(sm + L::OFF_SQ);
+      float ta = 0.f, tb = 0.f;
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int t = tid / kRows + 8 * half, i = tid % kRows;
-      if (t < K) {
-        float tot = 0.f;
-        for (int d = 0; d < kTiles * kWarps; ++d) tot += sSq[d * kKMax + t];
-        const float inv = rsqrtf(tot * (1.f / DV) + p.norm_eps);
-        const float zf = bf16_to_f32(uint16_t(half ? zz >> 16 : zz & 0xFFFFu));
-        const float y = sO[i * L::RSTRIDE + t] * inv * sm[L::OFF_NW + i] * silu(zf);
-        const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + i;
-        if (p.out_f32)
-          static_cast<float*>(p.out)[oi] = y;
-        else
-          static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(y);
+      for (int d = m; d < kTiles * kWarps; d += 4) {
+        const float2 v = sSq[d * (kKMax / 2) + cg];
+        ta += v.x;
+        tb += v.y;
+      }
+      ta += __shfl_xor_sync(0xffffffffu, ta, 8);
+      ta += __shfl_xor_sync(0xffffffffu, ta, 16);
+      tb += __shfl_xor_sync(0xffffffffu, tb, 8);
+      tb += __shfl_xor_sync(0xffffffffu, tb, 16);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int t = cg + 8 * half;
+        if (t < K) {
+          const float inv = rsqrtf((half ? tb : ta) * (1.f / DV) + p.norm_eps);
+          const float y = (half ? o_b : o_a) * inv * nw * silu(bf16_to_f32(half ? z_b : z_a));
+          const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
+          if (p.out_f32)
+            static_cast<float*>(p.out)[oi] = y;
+          else
+            static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(y);
+        }
       }
     }
   }
