@@ -584,7 +584,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   const int cg = lane & 7;   // column group (P) / token (outputs)
 
   // (a gated CTA's warps take part in the cluster exchange below even after a timeout)
-  float o_a = 0.f, o_b = 0.f;  // gated: o of (row m, tokens cg and cg + 8), normed at the end
+  // gated: o of (row m, tokens cg and cg + 8), scaled by w SiLU(z) once its square is taken, and
+  // the squares themselves
+  float o_a = 0.f, o_b = 0.f, sq_a = 0.f, sq_b = 0.f;
   if (ok) {
   (void)mbar_try_wait(bar, 0);  // every lane observes the completed phase
 
@@ -644,10 +646,14 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
       float o = p.q_scale * gGam[t] * sP[(row0 + m) * L::PSTRIDE + kKMax + t];
       for (int jj = 0; jj <= t; ++jj) o = fmaf(gN[t * kMStride + jj], sU[jj * kRowsPerWarp + m], o);
       if constexpr (kGated) {
-        if (half == 0)
-          o_a = o;
-        else
-          o_b = o;
+        const float gz = nw * silu(bf16_to_f32(half ? z_b : z_a));
+        if (half == 0) {
+          sq_a = o * o;
+          o_a = o * gz;
+        } else {
+          sq_b = o * o;
+          o_b = o * gz;
+        }
       } else {
         const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
         if (p.out_f32)
@@ -660,11 +666,11 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   __syncwarp();
   }  // ok
 
-  if constexpr (kGated) {
-    // sums of o^2 over the warp's 4 rows (lanes m = 0..3 of one column group), pushed into every
-    // CTA of the cluster as asynchronous stores that complete on the receiver's bar_sq; the
-    // sender never waits for them, the receiver only in its epilogue
-    float sq_a = o_a * o_a, sq_b = o_b * o_b;
+  // gated: the exchange of the sums of o^2 over the warp's 4 rows (lanes m = 0..3 of one column
+  // group), pushed into every CTA of the cluster as asynchronous stores that complete on the
+  // receiver's bar_sq, and the output norm that waits for them; both run inside the state stream
+  // (after its first and middle token) so that their latency hides behind the stores in flight
+  auto gated_push = [&]() {
     sq_a += __shfl_xor_sync(0xffffffffu, sq_a, 8);
     sq_a += __shfl_xor_sync(0xffffffffu, sq_a, 16);
     sq_b += __shfl_xor_sync(0xffffffffu, sq_b, 8);
@@ -676,7 +682,44 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
       const uint32_t sbar = smem_addr(bar_sq);
       for (int d = 0; d < kTiles; ++d) st_async_cluster_f32x2(map_to_rank(slot, d), sq_a, sq_b, map_to_rank(sbar, d));
     }
-  }
+  };
+  // out = o rsqrt(sum_rows o^2 / dv + eps) w SiLU(z) over the head's dv rows, which the cluster's
+  // kTiles CTAs share, per warp on the o w SiLU(z) it holds.  Every CTA waits here for all pushes
+  // into its shared memory, so none exits while a peer still writes to it.
+  auto gated_finish = [&]() {
+    const bool got = mbar_wait_bounded(bar_sq, 0);
+    if (!got && lane == 0) atomicOr(p.err, kDevErrTimeout);
+    if (ok && got) {
+      // lane (m, cg) adds the partials of warps m, m + 4, ...; the xor over the m bits completes
+      const float2* sSq = reinterpret_cast<const float2*>(sm + L::OFF_SQ);
+      float ta = 0.f, tb = 0.f;
+#pragma unroll
+      for (int d = m; d < kTiles * kWarps; d += 4) {
+        const float2 v = sSq[d * (kKMax / 2) + cg];
+        ta += v.x;
+        tb += v.y;
+      }
+      ta += __shfl_xor_sync(0xffffffffu, ta, 8);
+      ta += __shfl_xor_sync(0xffffffffu, ta, 16);
+      tb += __shfl_xor_sync(0xffffffffu, tb, 8);
+      tb += __shfl_xor_sync(0xffffffffu, tb, 16);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int t = cg + 8 * half;
+        if (t < K) {
+          const float inv = rsqrtf((half ? tb : ta) * (1.f / DV) + p.norm_eps);
+          const float y = (half ? o_b : o_a) * inv;
+          const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
+          if (p.out_f32)
+            static_cast<float*>(p.out)[oi] = y;
+          else
+            static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(y);
+        }
+      }
+    }
+  };
+  (void)gated_push;
+  (void)gated_finish;
 
   if (ok) {
   // stream the K states from registers: lane owns DK/32 float4 of the warp's 4 rows
@@ -749,43 +792,17 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
       else
         __stcs(d4, s[q]);
     }
+    if constexpr (kGated) {
+      if (t == 0) gated_push();
+      if (t == K / 2) gated_finish();
+    }
   }
   }  // ok
 
   if constexpr (kGated) {
-    // gated output norm over the head's dv rows, which the cluster's kTiles CTAs share:
-    // out = o rsqrt(sum_rows o^2 / dv + eps) w SiLU(z), per warp on the o values it holds.  Every
-    // CTA waits here for all pushes into its shared memory, so none exits while a peer still
-    // writes to it.
-    const bool got = mbar_wait_bounded(bar_sq, 0);
-    if (!got && lane == 0) atomicOr(p.err, kDevErrTimeout);
-    if (ok && got) {
-      // lane (m, cg) adds the partials of warps m, m + 4, ...; the xor over the m bits completes
-      const float2* sSq = reinterpret_cast<const float2*>(sm + L::OFF_SQ);
-      float ta = 0.f, tb = 0.f;
-#pragma unroll
-      for (int d = m; d < kTiles * kWarps; d += 4) {
-        const float2 v = sSq[d * (kKMax / 2) + cg];
-        ta += v.x;
-        tb += v.y;
-      }
-      ta += __shfl_xor_sync(0xffffffffu, ta, 8);
-      ta += __shfl_xor_sync(0xffffffffu, ta, 16);
-      tb += __shfl_xor_sync(0xffffffffu, tb, 8);
-      tb += __shfl_xor_sync(0xffffffffu, tb, 16);
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int t = cg + 8 * half;
-        if (t < K) {
-          const float inv = rsqrtf((half ? tb : ta) * (1.f / DV) + p.norm_eps);
-          const float y = (half ? o_b : o_a) * inv * nw * silu(bf16_to_f32(half ? z_b : z_a));
-          const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
-          if (p.out_f32)
-            static_cast<float*>(p.out)[oi] = y;
-          else
-            static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(y);
-        }
-      }
+    if (!ok) {  // (the exchange still runs: the peers wait for this CTA's partials)
+      gated_push();
+      gated_finish();
     }
   }
 }
