@@ -59,6 +59,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+// One arrival (release semantics at CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -214,6 +219,76 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) 
       "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// The 16x256b access shape, for the M = 64 accumulator layout (rows in lanes 0..15 of each
+// warp's 32-lane quarter): per repetition 16 lanes x 8 columns, thread t of the warp holding
+// lanes t/4 and t/4 + 8 at columns 2(t%4) and 2(t%4) + 1.  Value 4j + e of an x4 access at
+// column c: e = 0, 1 -> lane t/4, column c + 8j + 2(t%4) + e; e = 2, 3 -> lane t/4 + 8, the same
+// two columns.  Each helper issues its accesses and waits for them in one asm statement, so
+// that no register is touched while the access is in flight.
+#define GDN_R16(o) "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3]), "=r"(o[4]), "=r"(o[5]), "=r"(o[6]), "=r"(o[7]), \
+    "=r"(o[8]), "=r"(o[9]), "=r"(o[10]), "=r"(o[11]), "=r"(o[12]), "=r"(o[13]), "=r"(o[14]), "=r"(o[15])
+#define GDN_W16(o) "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3]), "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7]), \
+    "r"(o[8]), "r"(o[9]), "r"(o[10]), "r"(o[11]), "r"(o[12]), "r"(o[13]), "r"(o[14]), "r"(o[15])
+
+__device__ __forceinline__ void tmem_ld16x256_x4(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : GDN_R16(r)
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int q = 0; q < 16; ++q) v[q] = __uint_as_float(r[q]);
+}
+
+// two x4 accesses (any two column offsets), one wait
+__device__ __forceinline__ void tmem_ld16x256_2x4(uint32_t taddr0, uint32_t taddr1, float (&v0)[16], float (&v1)[16]) {
+  uint32_t r[16], s[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%32];\n\t"
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%33];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : GDN_R16(r), GDN_R16(s)
+      : "r"(taddr0), "r"(taddr1)
+      : "memory");
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    v0[q] = __uint_as_float(r[q]);
+    v1[q] = __uint_as_float(s[q]);
+  }
+}
+
+__device__ __forceinline__ void tmem_st16x256_x4(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      GDN_W16(r)
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16x256_2x4(uint32_t taddr0, uint32_t taddr1, const uint32_t (&r)[16],
+                                                  const uint32_t (&s)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};\n\t"
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%1], {%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr0),
+      "r"(taddr1), GDN_W16(r), GDN_W16(s)
+      : "memory");
+}
+#undef GDN_R16
+#undef GDN_W16
+
+// Two f32 values -> their bf16 hi parts and lo parts (hi = bf16(x), lo = bf16(x - hi)), each pair
+// packed into one 32-bit word, the first value in the low half.
+__device__ __forceinline__ void split2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 hb = __floats2bfloat162_rn(a, b);
+  const float2 hf = __bfloat1622float2(hb);
+  const __nv_bfloat162 lb = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&hb);
+  lo = *reinterpret_cast<const uint32_t*>(&lb);
 }
 
 // Eight f32 values x -> their bf16 parts hi = bf16(x), lo = bf16(x - hi), packed as two 16-byte

@@ -463,21 +463,35 @@ struct TcLayout {
   static constexpr int OFF_X = OFF_U + 2 * BLK;          // raw x [67][64] f32 (3 history rows)
   static constexpr int OFF_TAP = OFF_X + 67 * kTileRows * 4;  // conv taps [64][4]
   static constexpr int OFF_BAR = OFF_TAP + kTileRows * 16;    // mbarriers
-  static constexpr int NBAR = 10;
+  static constexpr int NBAR = 13;
   static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_TSLOT + 16;
   static_assert(OFF_TAP % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
 };
 
-// TMEM columns
-constexpr uint32_t kColS = 0, kColPk = 128, kColPq = 192, kColU = 256, kColO = 320, kTmemCols = 512;
+// TMEM columns: the state, two buffers of P = [P_k | P_q] (chunk parity), u, o'
+constexpr uint32_t kColS = 0, kColP0 = 128, kColU = 384, kColO = 448, kTmemCols = 512;
 // mbarriers
-enum { kBarKQ = 0, kBarKT, kBarW, kBarMQ, kBarGD0, kBarGD1, kBarPk, kBarU, kBarO, kBarS };
+enum { kBarKQ = 0, kBarKT, kBarW, kBarMQ, kBarGD0, kBarGD1, kBarPk, kBarU, kBarO, kBarS, kRdyR, kRdyU, kRdyS, kNumBars };
+constexpr uint32_t kEpiThreads = kThreads;  // arrivals on the kRdy* (operand written) barriers
 
 // every thread waits (bounded); true when any thread of the CTA gave up
 __device__ __forceinline__ bool wait_failed(uint64_t* bar, uint32_t parity) {
   const bool ok = mbar_wait_bounded(bar, parity);
   return __syncthreads_or(!ok) != 0;
+}
+
+// Named barrier 1 over the state kernel's 256 epilogue threads (warps 0..7), plain and with an
+// or-reduction of a predicate.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool epi_any(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(uint32_t(v))
+      : "memory");
+  return r != 0;
 }
 
 // One product of the chunk form as three bf16 MMA chains over hi/lo operand pairs (hi.hi, hi.lo,
@@ -498,6 +512,11 @@ __device__ __forceinline__ void umma_split3(uint32_t d, uint32_t a_hi, uint32_t 
   }
 }
 
+// Row-swizzled [rows][64] f32 tables (raw x, staged outputs): element (t, c) at t * 64 +
+// (c ^ swz(t)); the swizzle spreads the 16x256b thread layout's four token columns over all
+// banks and keeps groups of four consecutive c together.
+__device__ __forceinline__ int swz(int t) { return ((t >> 1) & 3) << 3; }
+
 constexpr int kIssuer = kThreads;  // the state kernel's copy / MMA issuing thread (first of warp 8)
 
 template <int DK, int DV>
@@ -505,6 +524,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
   using L = TcLayout<DK>;
   extern __shared__ __align__(128) uint8_t smb[];
   constexpr int kHalves = DV / kTileRows;
+  constexpr int SC = DK / 2;      // state columns per epilogue thread (two warps per row quarter)
+  constexpr int SREP = SC / 32;   // 16x256b x4 accesses per state half
+  static_assert(SREP == 1 || SREP == 2, "dk = 64 or 128");
+  static_assert(L::NBAR >= kNumBars, "mbarrier slots");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int i = blockIdx.y;
   const int h = blockIdx.x / kHalves;
@@ -522,15 +545,18 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
   uint32_t* tslot = reinterpret_cast<uint32_t*>(smb + L::OFF_TSLOT);
   const uint32_t sbase = smem_addr(smb);
 
-  // epilogue coordinates: row m of the tile (lanes 0..15), column half hh
+  // epilogue coordinates.  32x32b accesses (state in and out): row m (lanes 0..15), column half
+  // hh.  16x256b accesses (the chunk loop): rows ra, rb = ra + 8, columns 2 c4 + e of each
+  // 8-column block of the half.
   const int quad = warp & 3, hh = warp >> 2;
   const int m = 16 * quad + (lane & 15);
   const bool epi = warp < kThreads / 32;  // an epilogue warp (not the issuing warp)
   const bool act = epi && lane < 16;
   const uint32_t lane_sel = uint32_t(32 * quad) << 16;
+  const int ra = 16 * quad + (lane >> 2), rb = ra + 8, c4 = lane & 3;
 
   if (tid == 0) {
-    for (int q = 0; q < L::NBAR; ++q) mbar_init(bar + q, 1);
+    for (int q = 0; q < kNumBars; ++q) mbar_init(bar + q, q >= kRdyR ? kEpiThreads : 1);
     fence_mbar_init();
   }
   if (warp == 0) tmem_alloc(tslot, kTmemCols);
@@ -539,8 +565,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
   tc_fence_after();
   const uint32_t tmem = *tslot;
 
-  // phases armed per barrier (thread 0 only), so that a failed CTA can wait for what it started
-  int armed[L::NBAR] = {};
+  // phases armed per barrier (thread kIssuer only), so that a failed CTA can wait for what it started
+  int armed[kNumBars] = {};
   auto issue_kq = [&](int c) {
     ++armed[kBarKQ];
     mbar_arrive_expect_tx(bar + kBarKQ, 4 * L::BLK_KQ);
@@ -583,7 +609,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
     if (n_chunks > 1) issue_gd(1);
   }
 
-  // S hi/lo operand stores of this thread's columns [c0, c0 + n) of row m
+  // S hi/lo operand stores of this thread's columns [c0, c0 + n) of row m (32x32b layout)
   auto store_pair = [&](int off, int row, int k0, int kdim, const float* v, int n) {
     for (int q = 0; q < n; q += 8) {
       uint4 hi, lo;
@@ -593,9 +619,25 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
       *reinterpret_cast<uint4*>(smb + off + (kdim == DK ? L::BLK_KQ : L::BLK) + o) = lo;
     }
   };
+  // hi/lo operand stores of a 16x256b register block: 4 reps x (rows ra, rb) x 2 columns from
+  // column k0 of a K-major operand with kdim columns (lo block `lo_off` bytes after hi)
+  auto store_block = [&](int off, uint32_t lo_off, int k0, int kdim, const float (&v)[16]) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int k = k0 + 8 * j + 2 * c4;
+      uint32_t hi, lo;
+      split2(v[4 * j], v[4 * j + 1], hi, lo);
+      uint32_t o = kmajor_off(ra, k, kdim);
+      *reinterpret_cast<uint32_t*>(smb + off + o) = hi;
+      *reinterpret_cast<uint32_t*>(smb + off + lo_off + o) = lo;
+      split2(v[4 * j + 2], v[4 * j + 3], hi, lo);
+      o = kmajor_off(rb, k, kdim);
+      *reinterpret_cast<uint32_t*>(smb + off + o) = hi;
+      *reinterpret_cast<uint32_t*>(smb + off + lo_off + o) = lo;
+    }
+  };
 
   // the state tile into TMEM and, split, into the S operand; taps; the v channels' history
-  constexpr int SC = DK / 2;  // state columns per thread
   {
     const float* src = p.state_in + ((size_t(i) * p.Hv + h) * DV + r0 + m) * DK + hh * SC;
 #pragma unroll
@@ -612,7 +654,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
     if (tid < kTileRows) *reinterpret_cast<float4*>(sTap + 4 * tid) = *reinterpret_cast<const float4*>(p.conv_w + (vch0 + tid) * kConvW);
     for (int idx = tid; idx < 3 * kTileRows; idx += kThreads) {
       const int mm = idx / kTileRows, ch = idx % kTileRows;
-      sX[mm * kTileRows + ch] = p.conv_state_in[(size_t(i) * 3 + mm) * C + vch0 + ch];
+      sX[mm * kTileRows + (ch ^ swz(mm))] = p.conv_state_in[(size_t(i) * 3 + mm) * C + vch0 + ch];
     }
   }
   // raw x of the tile's 64 channels for one chunk: thread = (token tid / 4, 16 channels)
@@ -630,229 +672,308 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
 
   const uint32_t id_n64 = umma_idesc_bf16(kTileRows, kCh), id_ndk = umma_idesc_bf16(kTileRows, DK);
   const uint32_t id_n128 = umma_idesc_bf16(kTileRows, 2 * kCh);
-  // the state in TMEM is kept pre-scaled by the current chunk's Gamma_63, so that the update
-  // MMA can accumulate onto it; this thread's 32-column blocks of it:
-  auto scale_state = [&](const float* gam) {
-    const float gl = gam[kCh - 1];
-#pragma unroll
-    for (int c0 = 0; c0 < SC; c0 += 32) {
-      float sv[32];
-      tmem_ld32(tmem + lane_sel + kColS + hh * SC + c0, sv);
-#pragma unroll
-      for (int q = 0; q < 32; ++q) sv[q] *= gl;
-      tmem_st32(tmem + lane_sel + kColS + hh * SC + c0, sv);
-    }
-  };
   bool failed = false;
   if (n_chunks > 0) {
+    // the state in TMEM is kept pre-scaled by the current chunk's Gamma_63, so that the update
+    // MMA can accumulate onto it
     if (wait_failed(bar + kBarGD0, 0)) {
       failed = true;
     } else {
       tc_fence_after();
-      if (epi) scale_state(reinterpret_cast<const float*>(smb + L::OFF_GD));
-      tc_fence_before();
-      __syncthreads();
-      tc_fence_after();
-    }
-  }
-  int len = 0;
-  for (int lc = 0; lc < n_chunks && !failed; ++lc) {
-    const uint32_t par = lc & 1;
-    const float* sGam = reinterpret_cast<const float*>(smb + L::OFF_GD + (lc & 1) * 2 * kCh * 4);
-    const float* sd = sGam + kCh;
-    const long long tok0 = s0 + (long long)lc * kCh;
-    len = int(min_ll(kCh, s1 - tok0));
-
-    // (a) raw x of this chunk to rows 3..66; the next chunk's x is fetched meanwhile
-    if (tid < kThreads) {
-      const uint32_t wv[8] = {xr0.x, xr0.y, xr0.z, xr0.w, xr1.x, xr1.y, xr1.z, xr1.w};
-      float* row = sX + (xt + 3) * kTileRows + 16 * xg;
+      if (epi) {
+        const float gl = reinterpret_cast<const float*>(smb + L::OFF_GD)[kCh - 1];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        row[2 * q] = (xt < len) ? bf16_to_f32(uint16_t(wv[q] & 0xFFFFu)) : 0.f;
-        row[2 * q + 1] = (xt < len) ? bf16_to_f32(uint16_t(wv[q] >> 16)) : 0.f;
-      }
-      const long long nt = tok0 + kCh + xt;
-      if (lc + 1 < n_chunks && nt < s1) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + size_t(nt) * C + vch0 + 16 * xg);
-        xr0 = src[0];
-        xr1 = src[1];
-      }
-    }
-    __syncthreads();  // sX rows written
-    // (b) P = S [k^ | q^]^T on the tensor cores (k^ and q^ stacked as one N = 128 operand, the
-    // result in the adjacent P_k | P_q columns), while the threads run the conv of their row m
-    // (channel m) over their 32 tokens
-    if (tid == kIssuer) {
-      if (mbar_wait_bounded(bar + kBarKQ, par)) {
-        tc_fence_after();
-        const uint32_t sS = sbase + L::OFF_S, sKQ = sbase + L::OFF_KQ;
-        umma_split3<DK / 16>(tmem + kColPk, sS, sS + L::BLK_KQ, sKQ, sKQ + 2 * L::BLK_KQ, (DK / 8) * 128, id_n128,
-                             false);
-        umma_commit(bar + kBarPk);
-        ++armed[kBarPk];
-      }
-    }
-    float v[32];
-    if (act) {
-      const float4 w = *reinterpret_cast<const float4*>(sTap + 4 * m);
-#pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const int t = 32 * hh + q;
-        const float z = fmaf(w.w, sX[(t + 3) * kTileRows + m],
-                             fmaf(w.z, sX[(t + 2) * kTileRows + m], fmaf(w.y, sX[(t + 1) * kTileRows + m], w.x * sX[t * kTileRows + m])));
-        v[q] = silu(z);
-      }
-    }
-    if (wait_failed(bar + kBarPk, par)) {
-      failed = true;
-      break;
-    }
-    tc_fence_after();
-    // (c) r = v - Gamma o P_k -> operand
-    if (epi) {
-      float pk[32];
-      tmem_ld32(tmem + lane_sel + kColPk + 32 * hh, pk);
-      if (act) {
-#pragma unroll
-        for (int q = 0; q < 32; ++q) pk[q] = fmaf(-sGam[32 * hh + q], pk[q], v[q]);
-        store_pair(L::OFF_RD, m, 32 * hh, kCh, pk, 32);
-      }
-    }
-    // the last three raw rows become the next chunk's history (the conv is done with them)
-    if (len == kCh)
-      for (int idx = tid; idx < 3 * kTileRows; idx += kThreads + 32) sX[idx] = sX[kCh * kTileRows + idx];
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // (d) u = r W^T; once the q^ MMAs are done too, the next chunk's k^|q^ may come in
-    if (tid == kIssuer) {
-      if (mbar_wait_bounded(bar + kBarW, par)) {
-        tc_fence_after();
-        umma_split3<kCh / 16>(tmem + kColU, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK, sbase + L::OFF_W,
-                              sbase + L::OFF_W + L::BLK, 1024, id_n64, false);
-        umma_commit(bar + kBarU);
-        ++armed[kBarU];
-      }
-      if (lc + 1 < n_chunks) issue_kq(c_first + lc + 1);  // the P MMAs are done with k^, q^
-    }
-    if (wait_failed(bar + kBarU, par)) {
-      failed = true;
-      break;
-    }
-    tc_fence_after();
-    if (epi) {
-      float u[32];
-      tmem_ld32(tmem + lane_sel + kColU + 32 * hh, u);
-      if (act) {
-        store_pair(L::OFF_U, m, 32 * hh, kCh, u, 32);
-#pragma unroll
-        for (int q = 0; q < 32; ++q) u[q] *= sd[32 * hh + q];
-        store_pair(L::OFF_RD, m, 32 * hh, kCh, u, 32);  // r is dead: the u MMAs are done
-      }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // (e) o' = u MQ^T (own commit), then S += (d o u) k^
-    if (tid == kIssuer) {
-      if (lc + 1 < n_chunks) issue_w(c_first + lc + 1);
-      if (mbar_wait_bounded(bar + kBarMQ, par)) {
-        tc_fence_after();
-        umma_split3<kCh / 16>(tmem + kColO, sbase + L::OFF_U, sbase + L::OFF_U + L::BLK, sbase + L::OFF_MQ,
-                              sbase + L::OFF_MQ + L::BLK, 1024, id_n64, false);
-        umma_commit(bar + kBarO);
-        ++armed[kBarO];
-      }
-      if (mbar_wait_bounded(bar + kBarKT, par)) {
-        umma_split3<kCh / 16>(tmem + kColS, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK, sbase + L::OFF_KT,
-                              sbase + L::OFF_KT + L::BLK_KQ, 1024, id_ndk, true);
-        umma_commit(bar + kBarS);
-        ++armed[kBarS];
-      }
-    }
-    {
-      const bool ok = mbar_wait_bounded(bar + kBarO, par);
-      if (__syncthreads_or(!ok)) {
-        failed = true;
-        break;
-      }
-    }
-    tc_fence_after();
-    // outputs, while the state update runs: staged token-major in the u operand buffer (the o'
-    // MMAs are done with it) and written out after the next barrier as 16-byte stores
-    float* sOut = reinterpret_cast<float*>(smb + L::OFF_U);  // [64 tokens][64 rows]
-    if (epi) {
-      float o[32], pq[32];
-      tmem_ld32(tmem + lane_sel + kColO + 32 * hh, o);
-      tmem_ld32(tmem + lane_sel + kColPq + 32 * hh, pq);
-      if (act) {
-#pragma unroll
-        for (int q = 0; q < 32; ++q) sOut[(32 * hh + q) * kTileRows + m] = p.q_scale * fmaf(sGam[32 * hh + q], pq[q], o[q]);
-      }
-    }
-    // the new state: split into the S operand of the next chunk, and pre-scaled in TMEM by the
-    // next chunk's Gamma_63
-    const bool more = lc + 1 < n_chunks;
-    {
-      bool ok = mbar_wait_bounded(bar + kBarS, par);
-      if (more) ok = ok && mbar_wait_bounded(bar + kBarGD0 + ((lc + 1) & 1), ((lc + 1) >> 1) & 1);
-      if (__syncthreads_or(!ok)) {
-        failed = true;
-        break;
-      }
-    }
-    tc_fence_after();
-    if (tid < kThreads && xt < len) {  // thread = (token xt, rows 16 xg .. 16 xg + 15)
-      const float* src = sOut + xt * kTileRows + 16 * xg;
-      const size_t oi = size_t(tok0 + xt) * p.Hv * DV + size_t(h) * DV + r0 + 16 * xg;
-      if (p.out_f32) {
-        float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) o4[q] = *reinterpret_cast<const float4*>(src + 4 * q);
-      } else {
-        uint32_t w[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const __nv_bfloat162 b2 = __floats2bfloat162_rn(src[2 * q], src[2 * q + 1]);
-          w[q] = *reinterpret_cast<const uint32_t*>(&b2);
-        }
-        uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + oi);
-        o4[0] = make_uint4(w[0], w[1], w[2], w[3]);
-        o4[1] = make_uint4(w[4], w[5], w[6], w[7]);
-      }
-    }
-    if (epi) {
-      const float gl = more ? reinterpret_cast<const float*>(smb + L::OFF_GD + ((lc + 1) & 1) * 2 * kCh * 4)[kCh - 1] : 1.f;
-#pragma unroll
-      for (int c0 = 0; c0 < SC; c0 += 32) {
-        float sv[32];
-        tmem_ld32(tmem + lane_sel + kColS + hh * SC + c0, sv);
-        if (act) store_pair(L::OFF_S, m, hh * SC + c0, DK, sv, 32);
-        if (more) {
+        for (int c0 = 0; c0 < SC; c0 += 32) {
+          float sv[32];
+          tmem_ld32(tmem + lane_sel + kColS + hh * SC + c0, sv);
 #pragma unroll
           for (int q = 0; q < 32; ++q) sv[q] *= gl;
           tmem_st32(tmem + lane_sel + kColS + hh * SC + c0, sv);
         }
       }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == kIssuer && more) {
-      issue_mq(c_first + lc + 1);
-      issue_kt(c_first + lc + 1);
-      if (lc + 2 < n_chunks) issue_gd(lc + 2);
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
     }
   }
+
+  // From here the issuing thread and the epilogue warps run separate loops: the epilogue warps
+  // synchronise among themselves on named barrier 1 and hand each finished operand to the issuer
+  // through an mbarrier (256 arrivals), so that an issuer blocked on a full MMA queue never holds
+  // up an epilogue.
+  int len = 0;
+  if (tid == kIssuer) {
+    for (int lc = 0; lc < n_chunks && !failed; ++lc) {
+      const uint32_t par = lc & 1;
+      const uint32_t colP = kColP0 + 128 * par;
+      const bool more = lc + 1 < n_chunks;
+      const uint32_t sS = sbase + L::OFF_S, sKQ = sbase + L::OFF_KQ;
+      // P = S [k^ | q^]^T into this chunk's P buffer (k^ and q^ stacked as one N = 128 operand, the
+      // result in adjacent P_k | P_q columns), once the S operand is written.  One N = 128 MMA
+      // reads the A tile once for both halves: the M = 64 MMAs here are bound by shared-memory
+      // reads, not by the tensor core.
+      if ((lc > 0 && !mbar_wait_bounded(bar + kRdyS, (lc - 1) & 1)) || !mbar_wait_bounded(bar + kBarKQ, par)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      umma_split3<DK / 16>(tmem + colP, sS, sS + L::BLK_KQ, sKQ, sKQ + 2 * L::BLK_KQ, (DK / 8) * 128, id_n128, false);
+      umma_commit(bar + kBarPk);
+      ++armed[kBarPk];
+      // u = r W^T; the next chunk's k^|q^ once the q^ MMAs are done
+      if (!mbar_wait_bounded(bar + kRdyR, par) || !mbar_wait_bounded(bar + kBarW, par)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      umma_split3<kCh / 16>(tmem + kColU, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK, sbase + L::OFF_W,
+                            sbase + L::OFF_W + L::BLK, 1024, id_n64, false);
+      umma_commit(bar + kBarU);
+      ++armed[kBarU];
+      if (more) issue_kq(c_first + lc + 1);  // the P MMAs are done with k^, q^ (the epilogue waited)
+      // S += (d o u) k^ first (it heads the next chunk's chain), then o' = u MQ^T
+      if (!mbar_wait_bounded(bar + kRdyU, par)) {
+        failed = true;
+        break;
+      }
+      if (more) issue_w(c_first + lc + 1);        // the epilogue waited for the u MMAs
+      if (lc + 2 < n_chunks) issue_gd(lc + 2);    // chunk lc's Gamma and d are read
+      if (!mbar_wait_bounded(bar + kBarKT, par)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      umma_split3<kCh / 16>(tmem + kColS, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK, sbase + L::OFF_KT,
+                            sbase + L::OFF_KT + L::BLK_KQ, 1024, id_ndk, true);
+      umma_commit(bar + kBarS);
+      ++armed[kBarS];
+      if (!mbar_wait_bounded(bar + kBarMQ, par)) {
+        failed = true;
+        break;
+      }
+      umma_split3<kCh / 16>(tmem + kColO, sbase + L::OFF_U, sbase + L::OFF_U + L::BLK, sbase + L::OFF_MQ,
+                            sbase + L::OFF_MQ + L::BLK, 1024, id_n64, false);
+      umma_commit(bar + kBarO);
+      ++armed[kBarO];
+      if (more) {
+        if (!mbar_wait_bounded(bar + kBarS, par)) {
+          failed = true;
+          break;
+        }
+        issue_kt(c_first + lc + 1);
+        if (!mbar_wait_bounded(bar + kBarO, par)) {
+          failed = true;
+          break;
+        }
+        issue_mq(c_first + lc + 1);
+      }
+    }
+  } else if (epi && !failed && n_chunks > 0) {
+    // raw x of a chunk into rows 3..66 (zero past the prompt's end), then the next chunk's x is
+    // fetched: thread = (token xt, 16 channels)
+    auto stage_x = [&](long long tok0, int n) {
+      const uint32_t wv[8] = {xr0.x, xr0.y, xr0.z, xr0.w, xr1.x, xr1.y, xr1.z, xr1.w};
+      const int t = xt + 3, sw = swz(t);
+      float* row = sX + t * kTileRows;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float4 f;
+        f.x = (xt < n) ? bf16_to_f32(uint16_t(wv[2 * q] & 0xFFFFu)) : 0.f;
+        f.y = (xt < n) ? bf16_to_f32(uint16_t(wv[2 * q] >> 16)) : 0.f;
+        f.z = (xt < n) ? bf16_to_f32(uint16_t(wv[2 * q + 1] & 0xFFFFu)) : 0.f;
+        f.w = (xt < n) ? bf16_to_f32(uint16_t(wv[2 * q + 1] >> 16)) : 0.f;
+        *reinterpret_cast<float4*>(row + ((16 * xg + 4 * q) ^ sw)) = f;
+      }
+      const long long nt = tok0 + kCh + xt;
+      if (nt < s1) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + size_t(nt) * C + vch0 + 16 * xg);
+        xr0 = src[0];
+        xr1 = src[1];
+      }
+    };
+    // conv + SiLU of the v channels at this thread's (row, token) cells
+    float v[16];
+    auto conv = [&]() {
+      const float4 wa = *reinterpret_cast<const float4*>(sTap + 4 * ra);
+      const float4 wb = *reinterpret_cast<const float4*>(sTap + 4 * rb);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 32 * hh + 8 * j + 2 * c4 + (e & 1);
+          const int row = (e < 2) ? ra : rb;
+          const float4 w = (e < 2) ? wa : wb;
+          const float z = fmaf(w.w, sX[(t + 3) * kTileRows + (row ^ swz(t + 3))],
+                               fmaf(w.z, sX[(t + 2) * kTileRows + (row ^ swz(t + 2))],
+                                    fmaf(w.y, sX[(t + 1) * kTileRows + (row ^ swz(t + 1))],
+                                         w.x * sX[t * kTileRows + (row ^ swz(t))])));
+          v[4 * j + e] = silu(z);
+        }
+    };
+    // outputs o = q_scale (Gamma o P_q + o'), staged token-major in the u operand buffer (the o'
+    // MMAs are done with it), then written out as 16-byte stores
+    float* sOut = reinterpret_cast<float*>(smb + L::OFF_U);  // [64 tokens][64 rows], row-swizzled
+    auto out_chunk = [&](int lc, long long tok0, const float (&gam)[8]) {
+      float o[16], pq[16];
+      tmem_ld16x256_2x4(tmem + lane_sel + kColO + 32 * hh, tmem + lane_sel + kColP0 + 128 * (lc & 1) + kCh + 32 * hh, o,
+                        pq);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int t = 32 * hh + 8 * j + 2 * c4 + (e & 1);
+          const int row = (e < 2) ? ra : rb;
+          sOut[t * kTileRows + (row ^ swz(t))] = p.q_scale * fmaf(gam[2 * j + (e & 1)], pq[4 * j + e], o[4 * j + e]);
+        }
+      epi_sync();
+      if (xt < len) {  // thread = (token xt, rows 16 xg .. 16 xg + 15)
+        const float* src = sOut + xt * kTileRows;
+        const int sw = swz(xt);
+        const size_t oi = size_t(tok0 + xt) * p.Hv * DV + size_t(h) * DV + r0 + 16 * xg;
+        float4 f[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) f[q] = *reinterpret_cast<const float4*>(src + ((16 * xg + 4 * q) ^ sw));
+        if (p.out_f32) {
+          float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) o4[q] = f[q];
+        } else {
+          uint32_t w[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const __nv_bfloat162 b0 = __floats2bfloat162_rn(f[q].x, f[q].y);
+            const __nv_bfloat162 b1 = __floats2bfloat162_rn(f[q].z, f[q].w);
+            w[2 * q] = *reinterpret_cast<const uint32_t*>(&b0);
+            w[2 * q + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+          }
+          uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + oi);
+          o4[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          o4[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+      }
+    };
+    // every epilogue thread hands its operand writes to the tensor core and arrives
+    auto hand_over = [&](uint64_t* rdy) {
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(rdy);
+    };
+
+    stage_x(s0, int(min_ll(kCh, s1 - s0)));
+    epi_sync();
+    conv();
+    for (int lc = 0; lc < n_chunks; ++lc) {
+      const uint32_t par = lc & 1;
+      const uint32_t colP = kColP0 + 128 * par;
+      const float* sGam = reinterpret_cast<const float*>(smb + L::OFF_GD + (lc & 1) * 2 * kCh * 4);
+      const float* sd = sGam + kCh;
+      const long long tok0 = s0 + (long long)lc * kCh;
+      len = int(min_ll(kCh, s1 - tok0));
+      const bool more = lc + 1 < n_chunks;
+
+      // (a) r = v - Gamma o P_k -> operand; the last three raw rows become the next chunk's
+      // history (every conv read of this chunk is done: the barrier of the wait)
+      if (epi_any(!mbar_wait_bounded(bar + kBarPk, par))) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      float gam[8];
+      {
+        float pk[16];
+        tmem_ld16x256_x4(tmem + lane_sel + colP + 32 * hh, pk);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          gam[2 * j] = sGam[32 * hh + 8 * j + 2 * c4];
+          gam[2 * j + 1] = sGam[32 * hh + 8 * j + 2 * c4 + 1];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pk[4 * j + e] = fmaf(-gam[2 * j + (e & 1)], pk[4 * j + e], v[4 * j + e]);
+        }
+        store_block(L::OFF_RD, L::BLK, 32 * hh, kCh, pk);
+      }
+      if (len == kCh && tid < 3 * kTileRows) {
+        const int mm = tid / kTileRows, ch = tid % kTileRows;
+        sX[mm * kTileRows + (ch ^ swz(mm))] = sX[(kCh + mm) * kTileRows + (ch ^ swz(kCh + mm))];
+      }
+      hand_over(bar + kRdyR);
+      // (b) u and d o u -> operands
+      if (epi_any(!mbar_wait_bounded(bar + kBarU, par))) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      {
+        float u[16];
+        tmem_ld16x256_x4(tmem + lane_sel + kColU + 32 * hh, u);
+        store_block(L::OFF_U, L::BLK, 32 * hh, kCh, u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float d0 = sd[32 * hh + 8 * j + 2 * c4], d1 = sd[32 * hh + 8 * j + 2 * c4 + 1];
+          u[4 * j] *= d0;
+          u[4 * j + 1] *= d1;
+          u[4 * j + 2] *= d0;
+          u[4 * j + 3] *= d1;
+        }
+        store_block(L::OFF_RD, L::BLK, 32 * hh, kCh, u);  // r is dead: the u MMAs are done
+      }
+      hand_over(bar + kRdyU);
+      // (c) while the state update runs: the next chunk's raw x and conv
+      if (more) {
+        stage_x(tok0 + kCh, int(min_ll(kCh, s1 - tok0 - kCh)));
+        epi_sync();
+        conv();
+      }
+      // (d) the new state: split into the S operand of the next chunk, and pre-scaled in TMEM by
+      // the next chunk's Gamma_63
+      {
+        bool ok = mbar_wait_bounded(bar + kBarS, par);
+        if (more) ok = ok && mbar_wait_bounded(bar + kBarGD0 + ((lc + 1) & 1), ((lc + 1) >> 1) & 1);
+        if (epi_any(!ok)) {
+          failed = true;
+          break;
+        }
+      }
+      tc_fence_after();
+      {
+        const float gl = more ? reinterpret_cast<const float*>(smb + L::OFF_GD + ((lc + 1) & 1) * 2 * kCh * 4)[kCh - 1] : 1.f;
+        const uint32_t cs = tmem + lane_sel + kColS + hh * SC;
+        float sv[SREP][16];
+        if constexpr (SREP == 2)
+          tmem_ld16x256_2x4(cs, cs + 32, sv[0], sv[1]);
+        else
+          tmem_ld16x256_x4(cs, sv[0]);
+#pragma unroll
+        for (int q = 0; q < SREP; ++q) store_block(L::OFF_S, L::BLK_KQ, hh * SC + 32 * q, DK, sv[q]);
+        if (more) {
+          uint32_t w[SREP][16];
+#pragma unroll
+          for (int q = 0; q < SREP; ++q)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[q][e] = __float_as_uint(sv[q][e] * gl);
+          if constexpr (SREP == 2)
+            tmem_st16x256_2x4(cs, cs + 32, w[0], w[1]);
+          else
+            tmem_st16x256_x4(cs, w[0]);
+        }
+      }
+      hand_over(bar + kRdyS);
+      // (e) this chunk's outputs, while the next chunk's P runs
+      if (epi_any(!mbar_wait_bounded(bar + kBarO, par))) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      out_chunk(lc, tok0, gam);
+    }
+  }
+  // (the issuer's and the epilogue's failure flags meet here; warp 8's other lanes idled)
+  __syncwarp();
+  failed = __syncthreads_or(failed) != 0;
 
   if (failed) {
     if (tid == kIssuer) {  // one more bounded wait for every copy and MMA group still in flight
       atomicOr(p.err, kDevErrTimeout);
-      for (int q = 0; q < L::NBAR; ++q)
+      for (int q = 0; q < kNumBars; ++q)
         if (armed[q] > 0) (void)mbar_wait_bounded(bar + q, uint32_t(armed[q] - 1) & 1u);
     }
   } else {
@@ -867,10 +988,11 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
         for (int q = 0; q < 32; q += 4) *reinterpret_cast<float4*>(dst + c0 + q) = make_float4(sv[q], sv[q + 1], sv[q + 2], sv[q + 3]);
     }
     // conv history: the v channels from the last three raw rows (rows len .. len + 2 of the
-    // last chunk, or the untouched history of an empty prompt)
+    // last chunk, or the untouched history of an empty prompt); epilogue threads only, which
+    // know len
     for (int idx = tid; idx < 3 * kTileRows; idx += kThreads) {
       const int mm = idx / kTileRows, ch = idx % kTileRows;
-      p.conv_state_out[(size_t(i) * 3 + mm) * C + vch0 + ch] = sX[(len + mm) * kTileRows + ch];
+      p.conv_state_out[(size_t(i) * 3 + mm) * C + vch0 + ch] = sX[(len + mm) * kTileRows + (ch ^ swz(len + mm))];
     }
     // the q|k channels of the head group, split over the first v-head's row tiles; every value
     // is read before this thread writes, and no other thread of this grid reads them
