@@ -270,7 +270,7 @@ gdn_status gdn_prefill(const gdn_dims* dims, int64_t n_tokens, const int32_t* cu
 /*
  * Bytes of workspace gdn_prefill needs for `dims` (B, Hk, Hv, dk) and N tokens:
  * with cap = ceil(N / 64) + B chunks,
- * 16 ceil((B + 5) / 4) + cap (16 + Hk * 768 * dk + Hv * 33280).
+ * 16 ceil((B + 5) / 4) + cap (16 + Hk * 512 * dk + Hv * 33280).
  */
 gdn_status gdn_prefill_workspace_size(const gdn_dims* dims, int64_t n_tokens, uint64_t* bytes);
 

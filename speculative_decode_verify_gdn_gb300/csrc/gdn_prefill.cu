@@ -31,7 +31,7 @@ constexpr int kThreads = 256;
 constexpr int kCh = kPrefillChunk;   // 64 tokens per chunk
 constexpr int kAS = kCh + 1;         // row stride of the chunk kernel's 64 x 64 shared tables
 constexpr int kTileRows = 64;        // state rows per state-kernel CTA (the MMA M)
-constexpr int kKqBlocks = 6;         // k^ hi, lo, q^ hi, lo, k^T hi, lo per (chunk, q/k head)
+constexpr int kKqBlocks = 4;         // k^ hi, lo, q^ hi, lo per (chunk, q/k head)
 constexpr int kAbHeads = 8;          // v-heads per q/k head whose gate inputs the chunk kernel prefetches
 
 __device__ __forceinline__ float gate_beta(float b) { return 1.f / (1.f + expf(-b)); }
@@ -205,9 +205,9 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   __syncthreads();
 
   // normalised k^ and q^ to the workspace as bf16 hi/lo MMA operands (K-major core-matrix
-  // layout): k^ hi, q^ hi, k^ lo, q^ lo as [t][c] (K = DK; k^ and q^ adjacent, so that each pair
-  // reads as one 128-row operand), then k^ hi, lo transposed, [c][t] (K = 64).  Eight
-  // consecutive threads fill one 128-byte core matrix.
+  // layout, [t][c] with K = DK): k^ hi, k^ lo, q^ hi, q^ lo.  The state kernel also reads the k^
+  // blocks as the MN-major operand [c][t] of its state update.  Eight consecutive threads fill
+  // one 128-byte core matrix.
   {
     uint8_t* dst = reinterpret_cast<uint8_t*>(p.ws.kq) + (size_t(c) * p.Hk + kh) * kKqBlocks * (kCh * DK * 2);
     constexpr int BLK = kCh * DK * 2;
@@ -221,20 +221,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       uint4 hi, lo;
       split8(v, hi, lo);
       const uint32_t off = kmajor_off(t, 8 * cb, DK);
-      *reinterpret_cast<uint4*>(dst + part * BLK + off) = hi;
-      *reinterpret_cast<uint4*>(dst + (2 + part) * BLK + off) = lo;
-    }
-    for (int idx = tid; idx < DK * (kCh / 8); idx += kThreads) {
-      const int cm = idx >> 3, r8 = idx & 7;
-      const int ch = (cm / (kCh / 8)) * 8 + r8, tb = cm % (kCh / 8);
-      float v[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = sY[(8 * tb + q) * L::YS + DK + ch];
-      uint4 hi, lo;
-      split8(v, hi, lo);
-      const uint32_t off = kmajor_off(ch, 8 * tb, kCh);
-      *reinterpret_cast<uint4*>(dst + 4 * BLK + off) = hi;
-      *reinterpret_cast<uint4*>(dst + 5 * BLK + off) = lo;
+      *reinterpret_cast<uint4*>(dst + (2 * part) * BLK + off) = hi;
+      *reinterpret_cast<uint4*>(dst + (2 * part + 1) * BLK + off) = lo;
     }
   }
 
@@ -452,9 +440,11 @@ template <int DK>
 struct TcLayout {
   static constexpr int BLK_KQ = kCh * DK * 2;            // one 64 x DK bf16 operand
   static constexpr int BLK = kCh * kCh * 2;              // one 64 x 64 bf16 operand
-  static constexpr int OFF_KQ = 0;                       // k^ hi, lo, q^ hi, lo
-  static constexpr int OFF_KT = OFF_KQ + 4 * BLK_KQ;     // k^T hi, lo
-  static constexpr int OFF_W = OFF_KT + 2 * BLK_KQ;      // W hi, lo
+  // k^ of two chunks (buffers 0 and 1) around q^ of one: hi parts [k^0 | q^ | k^1], then the lo
+  // parts in the same order, so that k^ of either buffer and q^ are adjacent (one N = 128 operand)
+  static constexpr int OFF_KH = 0;
+  static constexpr int OFF_KL = OFF_KH + 3 * BLK_KQ;
+  static constexpr int OFF_W = OFF_KL + 3 * BLK_KQ;      // W hi, lo
   static constexpr int OFF_MQ = OFF_W + 2 * BLK;         // MQ hi, lo
   static constexpr int OFF_GD = OFF_MQ + 2 * BLK;        // two buffers of Gamma[64], d[64]
   static constexpr int OFF_S = OFF_GD + 2 * 2 * kCh * 4; // S hi, lo (64 x DK)
@@ -463,7 +453,7 @@ struct TcLayout {
   static constexpr int OFF_X = OFF_U + 2 * BLK;          // raw x [67][64] f32 (3 history rows)
   static constexpr int OFF_TAP = OFF_X + 67 * kTileRows * 4;  // conv taps [64][4]
   static constexpr int OFF_BAR = OFF_TAP + kTileRows * 16;    // mbarriers
-  static constexpr int NBAR = 13;
+  static constexpr int NBAR = 14;
   static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
   static constexpr int BYTES = OFF_TSLOT + 16;
   static_assert(OFF_TAP % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
@@ -472,7 +462,8 @@ struct TcLayout {
 // TMEM columns: the state, two buffers of P = [P_k | P_q] (chunk parity), u, o'
 constexpr uint32_t kColS = 0, kColP0 = 128, kColU = 384, kColO = 448, kTmemCols = 512;
 // mbarriers
-enum { kBarKQ = 0, kBarKT, kBarW, kBarMQ, kBarGD0, kBarGD1, kBarPk, kBarU, kBarO, kBarS, kRdyR, kRdyU, kRdyS, kNumBars };
+enum { kBarK0 = 0, kBarK1, kBarQ, kBarW, kBarMQ, kBarGD0, kBarGD1, kBarPk, kBarU, kBarO, kBarS, kRdyR, kRdyU, kRdyS,
+       kNumBars };
 constexpr uint32_t kEpiThreads = kThreads;  // arrivals on the kRdy* (operand written) barriers
 
 // every thread waits (bounded); true when any thread of the CTA gave up
@@ -509,6 +500,26 @@ __device__ __forceinline__ void umma_split3(uint32_t d, uint32_t a_hi, uint32_t 
 #pragma unroll
     for (int kk = 0; kk < KSTEPS; ++kk)
       umma_bf16(d, da + uint64_t(16 * kk), db + uint64_t(16 * kk), idesc, (accumulate || sp > 0 || kk > 0) ? 1u : 0u);
+  }
+}
+
+// The same with an MN-major B operand (the k^ blocks read as [c][t]): LBO is the byte step between
+// core matrices along K (eight tokens), SBO along N (eight channels), and a K step moves the B
+// start address by two core-matrix rows along K.
+template <int KSTEPS>
+__device__ __forceinline__ void umma_split3_bmn(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t a_sbo, uint32_t b_hi,
+                                                uint32_t b_lo, uint32_t b_lbo, uint32_t b_sbo, uint32_t idesc,
+                                                bool accumulate) {
+  const uint64_t dah = umma_smem_desc(a_hi, 128, a_sbo), dal = umma_smem_desc(a_lo, 128, a_sbo);
+  const uint64_t dbh = umma_smem_desc(b_hi, b_lbo, b_sbo), dbl = umma_smem_desc(b_lo, b_lbo, b_sbo);
+  const uint64_t bstep = uint64_t((2 * b_lbo) >> 4);
+#pragma unroll
+  for (int sp = 0; sp < 3; ++sp) {
+    const uint64_t da = (sp == 2) ? dal : dah;
+    const uint64_t db = (sp == 1) ? dbl : dbh;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk)
+      umma_bf16(d, da + uint64_t(16 * kk), db + bstep * kk, idesc, (accumulate || sp > 0 || kk > 0) ? 1u : 0u);
   }
 }
 
@@ -567,18 +578,20 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
 
   // phases armed per barrier (thread kIssuer only), so that a failed CTA can wait for what it started
   int armed[kNumBars] = {};
-  auto issue_kq = [&](int c) {
-    ++armed[kBarKQ];
-    mbar_arrive_expect_tx(bar + kBarKQ, 4 * L::BLK_KQ);
-    bulk_load(smb + L::OFF_KQ, reinterpret_cast<const uint8_t*>(p.ws.kq) + (size_t(c) * p.Hk + kh) * kKqBlocks * L::BLK_KQ,
-              4 * L::BLK_KQ, bar + kBarKQ);
+  auto kq_src = [&](int c) {
+    return reinterpret_cast<const uint8_t*>(p.ws.kq) + (size_t(c) * p.Hk + kh) * kKqBlocks * L::BLK_KQ;
   };
-  auto issue_kt = [&](int c) {
-    ++armed[kBarKT];
-    mbar_arrive_expect_tx(bar + kBarKT, 2 * L::BLK_KQ);
-    bulk_load(smb + L::OFF_KT,
-              reinterpret_cast<const uint8_t*>(p.ws.kq) + (size_t(c) * p.Hk + kh) * kKqBlocks * L::BLK_KQ + 4 * L::BLK_KQ,
-              2 * L::BLK_KQ, bar + kBarKT);
+  auto issue_k = [&](int c, int b) {  // k^ hi, lo of chunk c into buffer b
+    ++armed[kBarK0 + b];
+    mbar_arrive_expect_tx(bar + kBarK0 + b, 2 * L::BLK_KQ);
+    bulk_load(smb + L::OFF_KH + 2 * b * L::BLK_KQ, kq_src(c), L::BLK_KQ, bar + kBarK0 + b);
+    bulk_load(smb + L::OFF_KL + 2 * b * L::BLK_KQ, kq_src(c) + L::BLK_KQ, L::BLK_KQ, bar + kBarK0 + b);
+  };
+  auto issue_q = [&](int c) {
+    ++armed[kBarQ];
+    mbar_arrive_expect_tx(bar + kBarQ, 2 * L::BLK_KQ);
+    bulk_load(smb + L::OFF_KH + L::BLK_KQ, kq_src(c) + 2 * L::BLK_KQ, L::BLK_KQ, bar + kBarQ);
+    bulk_load(smb + L::OFF_KL + L::BLK_KQ, kq_src(c) + 3 * L::BLK_KQ, L::BLK_KQ, bar + kBarQ);
   };
   auto wq_src = [&](int c) {
     return reinterpret_cast<const uint8_t*>(p.ws.wm) + (size_t(c) * p.Hv + h) * (4 * L::BLK);
@@ -601,12 +614,15 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
               bar + kBarGD0 + b);
   };
   if (tid == kIssuer && n_chunks > 0) {
-    issue_kq(c_first);
-    issue_kt(c_first);
+    issue_k(c_first, 0);
+    issue_q(c_first);
     issue_w(c_first);
     issue_mq(c_first);
     issue_gd(0);
-    if (n_chunks > 1) issue_gd(1);
+    if (n_chunks > 1) {
+      issue_gd(1);
+      issue_k(c_first + 1, 1);
+    }
   }
 
   // S hi/lo operand stores of this thread's columns [c0, c0 + n) of row m (32x32b layout)
@@ -672,6 +688,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
 
   const uint32_t id_n64 = umma_idesc_bf16(kTileRows, kCh), id_ndk = umma_idesc_bf16(kTileRows, DK);
   const uint32_t id_n128 = umma_idesc_bf16(kTileRows, 2 * kCh);
+  const uint32_t id_ndk_bmn = id_ndk | (1u << 16);  // B MN-major
   bool failed = false;
   if (n_chunks > 0) {
     // the state in TMEM is kept pre-scaled by the current chunk's Gamma_63, so that the update
@@ -707,20 +724,33 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
       const uint32_t par = lc & 1;
       const uint32_t colP = kColP0 + 128 * par;
       const bool more = lc + 1 < n_chunks;
-      const uint32_t sS = sbase + L::OFF_S, sKQ = sbase + L::OFF_KQ;
-      // P = S [k^ | q^]^T into this chunk's P buffer (k^ and q^ stacked as one N = 128 operand, the
-      // result in adjacent P_k | P_q columns), once the S operand is written.  One N = 128 MMA
-      // reads the A tile once for both halves: the M = 64 MMAs here are bound by shared-memory
-      // reads, not by the tensor core.
-      if ((lc > 0 && !mbar_wait_bounded(bar + kRdyS, (lc - 1) & 1)) || !mbar_wait_bounded(bar + kBarKQ, par)) {
+      // P = S [k^ | q^]^T into this chunk's P buffer, once the S operand is written: k^ (buffer
+      // lc & 1) and q^ are adjacent, so they read as one N = 128 operand ([k^0 | q^] for even
+      // chunks, P_k in the first 64 columns; [q^ | k^1] for odd ones, P_k in the second 64).  One
+      // N = 128 MMA reads the A tile once for both halves: the M = 64 MMAs here are bound by
+      // shared-memory reads, not by the tensor core.
+      if ((lc > 0 && !mbar_wait_bounded(bar + kRdyS, (lc - 1) & 1)) ||
+          !mbar_wait_bounded(bar + kBarK0 + par, (lc >> 1) & 1) || !mbar_wait_bounded(bar + kBarQ, par)) {
         failed = true;
         break;
       }
       tc_fence_after();
-      umma_split3<DK / 16>(tmem + colP, sS, sS + L::BLK_KQ, sKQ, sKQ + 2 * L::BLK_KQ, (DK / 8) * 128, id_n128, false);
-      umma_commit(bar + kBarPk);
-      ++armed[kBarPk];
-      // u = r W^T; the next chunk's k^|q^ once the q^ MMAs are done
+      {
+        const uint32_t sS = sbase + L::OFF_S, bo = (par ? 1 : 0) * L::BLK_KQ;
+        umma_split3<DK / 16>(tmem + colP, sS, sS + L::BLK_KQ, sbase + L::OFF_KH + bo, sbase + L::OFF_KL + bo,
+                             (DK / 8) * 128, id_n128, false);
+        umma_commit(bar + kBarPk);
+        ++armed[kBarPk];
+      }
+      // the previous chunk's o' MMAs are done with MQ by now: this chunk's MQ comes in
+      if (lc > 0) {
+        if (!mbar_wait_bounded(bar + kBarO, (lc - 1) & 1)) {
+          failed = true;
+          break;
+        }
+        issue_mq(c_first + lc);
+      }
+      // u = r W^T; the next chunk's q^ (the P MMAs are done with it: the epilogue waited)
       if (!mbar_wait_bounded(bar + kRdyR, par) || !mbar_wait_bounded(bar + kBarW, par)) {
         failed = true;
         break;
@@ -730,21 +760,18 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
                             sbase + L::OFF_W + L::BLK, 1024, id_n64, false);
       umma_commit(bar + kBarU);
       ++armed[kBarU];
-      if (more) issue_kq(c_first + lc + 1);  // the P MMAs are done with k^, q^ (the epilogue waited)
-      // S += (d o u) k^ first (it heads the next chunk's chain), then o' = u MQ^T
+      if (more) issue_q(c_first + lc + 1);
+      // S += (d o u) k^ (k^ of this chunk's buffer, read MN-major), then o' = u MQ^T
       if (!mbar_wait_bounded(bar + kRdyU, par)) {
         failed = true;
         break;
       }
       if (more) issue_w(c_first + lc + 1);        // the epilogue waited for the u MMAs
       if (lc + 2 < n_chunks) issue_gd(lc + 2);    // chunk lc's Gamma and d are read
-      if (!mbar_wait_bounded(bar + kBarKT, par)) {
-        failed = true;
-        break;
-      }
       tc_fence_after();
-      umma_split3<kCh / 16>(tmem + kColS, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK, sbase + L::OFF_KT,
-                            sbase + L::OFF_KT + L::BLK_KQ, 1024, id_ndk, true);
+      umma_split3_bmn<kCh / 16>(tmem + kColS, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK, 1024,
+                                sbase + L::OFF_KH + 2 * par * L::BLK_KQ, sbase + L::OFF_KL + 2 * par * L::BLK_KQ,
+                                (DK / 8) * 128, 128, id_ndk_bmn, true);
       umma_commit(bar + kBarS);
       ++armed[kBarS];
       if (!mbar_wait_bounded(bar + kBarMQ, par)) {
@@ -755,17 +782,13 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
                             sbase + L::OFF_MQ + L::BLK, 1024, id_n64, false);
       umma_commit(bar + kBarO);
       ++armed[kBarO];
-      if (more) {
+      // k^ of chunk lc + 2 into this chunk's buffer once the update MMAs are done with it
+      if (lc + 2 < n_chunks) {
         if (!mbar_wait_bounded(bar + kBarS, par)) {
           failed = true;
           break;
         }
-        issue_kt(c_first + lc + 1);
-        if (!mbar_wait_bounded(bar + kBarO, par)) {
-          failed = true;
-          break;
-        }
-        issue_mq(c_first + lc + 1);
+        issue_k(c_first + lc + 2, par);
       }
     }
   } else if (epi && !failed && n_chunks > 0) {
@@ -815,8 +838,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
     float* sOut = reinterpret_cast<float*>(smb + L::OFF_U);  // [64 tokens][64 rows], row-swizzled
     auto out_chunk = [&](int lc, long long tok0, const float (&gam)[8]) {
       float o[16], pq[16];
-      tmem_ld16x256_2x4(tmem + lane_sel + kColO + 32 * hh, tmem + lane_sel + kColP0 + 128 * (lc & 1) + kCh + 32 * hh, o,
-                        pq);
+      tmem_ld16x256_2x4(tmem + lane_sel + kColO + 32 * hh,
+                        tmem + lane_sel + kColP0 + 128 * (lc & 1) + ((lc & 1) ? 0 : kCh) + 32 * hh, o, pq);
 #pragma unroll
       for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -881,7 +904,7 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
       float gam[8];
       {
         float pk[16];
-        tmem_ld16x256_x4(tmem + lane_sel + colP + 32 * hh, pk);
+        tmem_ld16x256_x4(tmem + lane_sel + colP + (par ? kCh : 0) + 32 * hh, pk);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           gam[2 * j] = sGam[32 * hh + 8 * j + 2 * c4];

@@ -212,7 +212,7 @@ def test_prefill_validation(lib):
     need = ctypes.c_uint64(0)
     assert lib.gdn_prefill_workspace_size(ctypes.byref(dims), ctypes.c_int64(N), ctypes.byref(need)) == gdn.GDN_OK
     cap = (N + 63) // 64 + dims.B
-    expect = 16 * ((dims.B + 5 + 3) // 4) + cap * (16 + dims.Hk * 768 * dims.dk + dims.Hv * 33280)
+    expect = 16 * ((dims.B + 5 + 3) // 4) + cap * (16 + dims.Hk * 512 * dims.dk + dims.Hv * 33280)
     assert need.value == expect
 
 
