@@ -136,38 +136,48 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   // channel reads its column into registers and walks the chunk.  The three rows before the
   // chunk come from the prompt itself or, at its start, from the history.
   float* sY = sm + L::OFF_Y;
+  static_assert(2 * DK <= kThreads, "one thread per q|k channel");
+  const int ch = tid;  // (threads beyond the 2 DK channels only join the barriers)
+  const bool own = ch < 2 * DK;
+  const size_t gch = (ch < DK) ? size_t(kh) * DK + ch : size_t(p.Hk) * DK + size_t(kh) * DK + (ch - DK);
+  float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+  float h[3] = {0.f, 0.f, 0.f};
   {
+    // every load of the tile, and the channel's taps and history, in flight at once
     uint16_t* sXr = reinterpret_cast<uint16_t*>(sY);
     constexpr int V8 = 2 * DK / 8;  // 16-byte groups per token row
-    for (int idx = tid; idx < kCh * V8; idx += kThreads) {
+    constexpr int kPer = kCh * V8 / kThreads;
+    static_assert(kCh * V8 % kThreads == 0, "whole 16-byte groups per thread");
+    uint4 v[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int idx = tid + q * kThreads;
       const int t = idx / V8, ch0 = 8 * (idx % V8);
       const size_t gch0 = (ch0 < DK) ? size_t(kh) * DK + ch0 : size_t(p.Hk) * DK + size_t(kh) * DK + (ch0 - DK);
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t < len) v = *reinterpret_cast<const uint4*>(p.x + size_t(tok0 + t) * C + gch0);
-      *reinterpret_cast<uint4*>(sXr + t * 2 * DK + ch0) = v;
+      v[q] = make_uint4(0, 0, 0, 0);
+      if (t < len) v[q] = *reinterpret_cast<const uint4*>(p.x + size_t(tok0 + t) * C + gch0);
     }
-  }
-  __syncthreads();
-  static_assert(2 * DK <= kThreads, "one thread per q|k channel");
-  {
-    const int ch = tid;  // (threads beyond the 2 DK channels only join the barriers)
-    const bool own = ch < 2 * DK;
-    const size_t gch = (ch < DK) ? size_t(kh) * DK + ch : size_t(p.Hk) * DK + size_t(kh) * DK + (ch - DK);
-    float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-    float h0 = 0.f, h1 = 0.f, h2 = 0.f;
-    uint16_t xs[kCh];
     if (own) {
       w = *reinterpret_cast<const float4*>(p.conv_w + gch * kConvW);
-      float h[3];
 #pragma unroll
       for (int m = 0; m < 3; ++m) {
         const long long pos = tok0 - 3 + m;
         h[m] = (pos >= s0) ? bf16_to_f32(p.x[size_t(pos) * C + gch])
                            : p.conv_state_in[(size_t(i) * 3 + size_t(pos - s0 + 3)) * C + gch];
       }
-      h0 = h[0];
-      h1 = h[1];
-      h2 = h[2];
+    }
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int idx = tid + q * kThreads;
+      const int t = idx / V8, ch0 = 8 * (idx % V8);
+      *reinterpret_cast<uint4*>(sXr + t * 2 * DK + ch0) = v[q];
+    }
+  }
+  __syncthreads();
+  {
+    float h0 = h[0], h1 = h[1], h2 = h[2];
+    uint16_t xs[kCh];
+    if (own) {
       const uint16_t* sXr = reinterpret_cast<const uint16_t*>(sY);
 #pragma unroll
       for (int t = 0; t < kCh; ++t) xs[t] = sXr[t * 2 * DK + ch];
@@ -742,15 +752,25 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
         umma_commit(bar + kBarPk);
         ++armed[kBarPk];
       }
-      // the previous chunk's o' MMAs are done with MQ by now: this chunk's MQ comes in
+      // Bulk copies are issued only right after an MMA group, while it runs: issuing one can hold
+      // this thread for hundreds of cycles, which must not delay the next MMA group.  The
+      // previous chunk's o' and update MMAs are done by now: this chunk's MQ, and the next
+      // chunk's k^ into the buffer the previous chunk used.
       if (lc > 0) {
         if (!mbar_wait_bounded(bar + kBarO, (lc - 1) & 1)) {
           failed = true;
           break;
         }
         issue_mq(c_first + lc);
+        if (more) {
+          if (!mbar_wait_bounded(bar + kBarS, (lc - 1) & 1)) {
+            failed = true;
+            break;
+          }
+          issue_k(c_first + lc + 1, (lc + 1) & 1);
+        }
       }
-      // u = r W^T; the next chunk's q^ (the P MMAs are done with it: the epilogue waited)
+      // u = r W^T; then the next chunk's q^ (the P MMAs are done with it: the epilogue waited)
       if (!mbar_wait_bounded(bar + kRdyR, par) || !mbar_wait_bounded(bar + kBarW, par)) {
         failed = true;
         break;
@@ -761,13 +781,13 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
       umma_commit(bar + kBarU);
       ++armed[kBarU];
       if (more) issue_q(c_first + lc + 1);
-      // S += (d o u) k^ (k^ of this chunk's buffer, read MN-major), then o' = u MQ^T
+      // S += (d o u) k^ (k^ of this chunk's buffer, read MN-major), then o' = u MQ^T; then the
+      // next chunk's W (the epilogue waited for the u MMAs) and Gamma, d of chunk lc + 2
+      // (chunk lc's are read)
       if (!mbar_wait_bounded(bar + kRdyU, par)) {
         failed = true;
         break;
       }
-      if (more) issue_w(c_first + lc + 1);        // the epilogue waited for the u MMAs
-      if (lc + 2 < n_chunks) issue_gd(lc + 2);    // chunk lc's Gamma and d are read
       tc_fence_after();
       umma_split3_bmn<kCh / 16>(tmem + kColS, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK, 1024,
                                 sbase + L::OFF_KH + 2 * par * L::BLK_KQ, sbase + L::OFF_KL + 2 * par * L::BLK_KQ,
@@ -782,14 +802,8 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
                             sbase + L::OFF_MQ + L::BLK, 1024, id_n64, false);
       umma_commit(bar + kBarO);
       ++armed[kBarO];
-      // k^ of chunk lc + 2 into this chunk's buffer once the update MMAs are done with it
-      if (lc + 2 < n_chunks) {
-        if (!mbar_wait_bounded(bar + kBarS, par)) {
-          failed = true;
-          break;
-        }
-        issue_k(c_first + lc + 2, par);
-      }
+      if (more) issue_w(c_first + lc + 1);
+      if (lc + 2 < n_chunks) issue_gd(lc + 2);
     }
   } else if (epi && !failed && n_chunks > 0) {
     // raw x of a chunk into rows 3..66 (zero past the prompt's end), then the next chunk's x is
