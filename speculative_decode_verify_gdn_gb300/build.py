@@ -53,9 +53,43 @@ def _digest() -> str:
     return h.hexdigest()
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without its comments and with blank runs collapsed (string and
+    character literals kept as they are)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_digest() -> str:
-    """Hash of the CUDA sources and flags (identifies the kernels a profile was taken on)."""
-    return _digest()[:16]
+    """Hash of the CUDA sources without their comments, and of the flags: identifies the
+    kernels a profile was taken on, and stays put when only commentary changes."""
+    h = hashlib.sha256()
+    files = sources() + sorted(os.path.join(CSRC_DIR, f) for f in os.listdir(CSRC_DIR)
+                               if f.endswith((".cuh", ".h"))) + [HEADER]
+    for f in files:
+        h.update(os.path.basename(f).encode())
+        with open(f, encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
+    h.update(" ".join(NVCC_FLAGS).encode())
+    return h.hexdigest()[:16]
 
 
 def build_library(force: bool = False, verbose: bool = False) -> str:

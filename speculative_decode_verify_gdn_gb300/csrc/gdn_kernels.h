@@ -105,7 +105,7 @@ inline long long prefill_chunk_cap(int B, long long N) { return (N + kPrefillChu
 // K-major core-matrix layout of 8 rows x 16 bytes):
 //   meta [4 + B + 1] int32     valid flag, chunk count, -, -, first chunk of each prompt (+ total)
 //   chunks [cap] int4          per chunk: prompt, first token, tokens (1..64), first token of the prompt
-//   kq   [cap][Hk][6][64 x dk] k^ hi, k^ lo, q^ hi, q^ lo as [t][c]; k^ hi, lo as [c][t]
+//   kq   [cap][Hk][4][64 x dk] k^ hi, k^ lo, q^ hi, q^ lo as [t][c] (k^ also read as [c][t])
 //   wm   [cap][Hv][4][64 x 64] W hi, W lo, MQ hi, MQ lo as [t][j]
 //   gd   [cap][Hv][2][64] f32  Gamma_t, then d_t = prod_{t<m<64} g_m
 struct PrefillWorkspace {

@@ -15,10 +15,10 @@
 //   gdn_prefill_chunk_kernel   one CTA per (chunk, q/k head), all chunks in parallel: conv of the
 //                              q|k channels, L2 norms, Gram products, gates, decay products and
 //                              the 64 x 64 triangular inverse of every v-head of the group;
-//   gdn_prefill_state_kernel   one CTA per (prompt, v-head, 32 state rows): walks the prompt's
-//                              chunks in order with the state tile in shared memory, the next
-//                              chunk's tables arriving by bulk copy (double-buffered) while
-//                              the current one is computed; convolves its own v channels.
+//   gdn_prefill_state_kernel   one CTA per (prompt, v-head, 64 state rows): walks the prompt's
+//                              chunks in order on the tensor cores with the state in tensor
+//                              memory, the next chunk's operands arriving by bulk copy while the
+//                              current one is computed; convolves its own v channels.
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 
@@ -441,11 +441,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
 // MMAs over hi/lo operand pairs (hi.hi + hi.lo + lo.hi), about 2^-16 relative per product:
 //   P  = S [k^ | q^]^T   (A = S hi/lo in shared memory, B = k^ / q^ hi/lo from kernel 1)
 //   u  = r W^T           (r = v - Gamma o P_k, written by the threads)
+//   S  = Gamma_63 S + (d o u) k^   (accumulated into the TMEM state, B = the k^ blocks read
+//                                   MN-major)
 //   o' = u MQ^T          (out = q_scale (Gamma o P_q + o'))
-//   S  = Gamma_63 S + (d o u) k^   (accumulated into the TMEM state, B = k^T hi/lo)
-// Thread roles: warps 0..7 run the epilogues (lanes 0..15 of warp w hold state row
-// 16 (w % 4) + lane, warps w and w + 4 splitting the columns); a ninth warp's first thread issues
-// the bulk copies and the MMAs, so that its stalls on the MMA queue delay no epilogue.
+// Thread roles: warps 0..7 run the epilogues (warp w reaches TMEM lanes 32 (w % 4) ..; warps w
+// and w + 4 split the columns); a ninth warp's first thread issues the bulk copies and the
+// MMAs in a loop of its own, so that its stalls on the MMA queue delay no epilogue.
 template <int DK>
 struct TcLayout {
   static constexpr int BLK_KQ = kCh * DK * 2;            // one 64 x DK bf16 operand
