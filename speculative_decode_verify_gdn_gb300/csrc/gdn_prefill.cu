@@ -93,6 +93,7 @@ __global__ void __launch_bounds__(1024) gdn_prefill_index_kernel(const PrefillPa
 template <int DK>
 struct ChunkLayout {
   static constexpr int YS = 2 * DK + 4;                       // row stride of the q|k conv table
+  static_assert(YS % 4 == 0, "16-byte rows");
   static constexpr int Y_FLOATS = kCh * YS;
   static constexpr int MAT = kCh * kAS;                       // one 64 x 65 matrix
   static constexpr int OFF_Y = 0;                             // [64][YS]: q (0..DK-1) | k (DK..2DK-1)
@@ -197,19 +198,36 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   }
   __syncthreads();
 
-  // a2: one warp per (token, q|k) vector
+  // a2: one warp per (token, q|k) vector, four vectors of a warp in flight together so that
+  // their shuffle reductions overlap
   {
     const int warp = tid >> 5, lane = tid & 31;
-    for (int v = warp; v < 2 * kCh; v += kThreads / 32) {
-      const int t = v >> 1, off = (v & 1) * DK;
-      float* row = sY + t * L::YS + off;
-      float ss = 0.f;
+    constexpr int kWarpsC = kThreads / 32;
+    constexpr int kPerWarp = 2 * kCh / kWarpsC;
+    static_assert(kPerWarp % 4 == 0, "four vectors at a time");
+    for (int k0 = 0; k0 < kPerWarp; k0 += 4) {
+      float x[4][DK / 32], ss[4];
 #pragma unroll
-      for (int e = lane; e < DK; e += 32) ss = fmaf(row[e], row[e], ss);
-      ss = warp_sum(ss);
-      const float inv = (t < len) ? rsqrtf(ss + p.l2_eps) : 0.f;
+      for (int u = 0; u < 4; ++u) {
+        const int v = warp + (k0 + u) * kWarpsC;
+        const float* row = sY + (v >> 1) * L::YS + (v & 1) * DK;
+        ss[u] = 0.f;
 #pragma unroll
-      for (int e = lane; e < DK; e += 32) row[e] *= inv;
+        for (int e = 0; e < DK / 32; ++e) {
+          x[u][e] = row[lane + 32 * e];
+          ss[u] = fmaf(x[u][e], x[u][e], ss[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) ss[u] = warp_sum(ss[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int v = warp + (k0 + u) * kWarpsC, t = v >> 1;
+        float* row = sY + t * L::YS + (v & 1) * DK;
+        const float inv = (t < len) ? rsqrtf(ss[u] + p.l2_eps) : 0.f;
+#pragma unroll
+        for (int e = 0; e < DK / 32; ++e) row[lane + 32 * e] = x[u][e] * inv;
+      }
     }
   }
   __syncthreads();
@@ -226,8 +244,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       const int cm = (idx >> 3) % (kCh * DK / 64), r8 = idx & 7;
       const int t = (cm / (DK / 8)) * 8 + r8, cb = cm % (DK / 8);
       float v[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) v[q] = sY[t * L::YS + (part ? 0 : DK) + 8 * cb + q];
+      {  // (16-byte aligned: YS and DK are multiples of 4)
+        const float4* src = reinterpret_cast<const float4*>(sY + t * L::YS + (part ? 0 : DK) + 8 * cb);
+        const float4 a0 = src[0], a1 = src[1];
+        v[0] = a0.x; v[1] = a0.y; v[2] = a0.z; v[3] = a0.w;
+        v[4] = a1.x; v[5] = a1.y; v[6] = a1.z; v[7] = a1.w;
+      }
       uint4 hi, lo;
       split8(v, hi, lo);
       const uint32_t off = kmajor_off(t, 8 * cb, DK);
