@@ -339,10 +339,12 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
     }
     __syncthreads();
     // decay products D[t][j] = prod_{j<m<=t} g_m = exp(G_t - G_j) on and below the diagonal,
-    // zeros above it (the blocked inverse relies on them); Gamma_t = exp(G_t)
+    // zeros above it (the blocked inverse relies on them); Gamma_t = exp(G_t).  The exponent is
+    // never positive, where the hardware exp2 path (__expf) is within a few ulps: far inside the
+    // 2^-16 of the hi/lo MMA products these entries feed.
     for (int idx = tid; idx < kCh * kCh; idx += kThreads) {
       const int t = idx / kCh, j = idx % kCh;
-      sD[t * kAS + j] = (j <= t) ? expf(sG[t] - sG[j]) : 0.f;
+      sD[t * kAS + j] = (j <= t) ? __expf(sG[t] - sG[j]) : 0.f;
     }
     if (tid < kCh) sGam[tid] = expf(sG[tid]);
     __syncthreads();
