@@ -88,6 +88,24 @@ __global__ void __launch_bounds__(1024) gdn_prefill_index_kernel(const PrefillPa
   }
 }
 
+// One product of the chunk form as three bf16 MMA chains over hi/lo operand pairs (hi.hi, hi.lo,
+// lo.hi) of KSTEPS steps of K = 16 each.  Descriptors are formed once; a K step moves the start
+// address field by 256 bytes (two core matrices).
+template <int KSTEPS>
+__device__ __forceinline__ void umma_split3(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
+                                            uint32_t sbo, uint32_t idesc, bool accumulate) {
+  const uint64_t dah = umma_smem_desc(a_hi, 128, sbo), dal = umma_smem_desc(a_lo, 128, sbo);
+  const uint64_t dbh = umma_smem_desc(b_hi, 128, sbo), dbl = umma_smem_desc(b_lo, 128, sbo);
+#pragma unroll
+  for (int sp = 0; sp < 3; ++sp) {
+    const uint64_t da = (sp == 2) ? dal : dah;
+    const uint64_t db = (sp == 1) ? dbl : dbh;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk)
+      umma_bf16(d, da + uint64_t(16 * kk), db + uint64_t(16 * kk), idesc, (accumulate || sp > 0 || kk > 0) ? 1u : 0u);
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // Kernel 1: per (chunk, q/k head).
 template <int DK>
@@ -105,7 +123,9 @@ struct ChunkLayout {
   static constexpr int OFF_BG = OFF_QK + MAT;                 // beta[64], G[64] (sum of log g), Gamma[64]
   static constexpr int OFF_Y2 = OFF_BG + 3 * kCh;             // [32][33] product temp of the inverse
   static constexpr int OFF_AB = OFF_Y2 + 32 * 33;             // a, b of the first kAbHeads v-heads [e][2][64]
-  static constexpr int FLOATS = OFF_AB + kAbHeads * 2 * kCh;
+  static constexpr int OFF_BAR = (OFF_AB + kAbHeads * 2 * kCh + 1) & ~1;  // 2 mbarriers, the TMEM slot
+  static constexpr int FLOATS = OFF_BAR + 6;
+  static_assert(4 * kCh * DK * 2 <= R_FLOATS * 4, "the split q|k operands fit in the conv table's space");
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
 };
 
@@ -117,6 +137,14 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   const int c = blockIdx.x;
   const int kh = blockIdx.y;
   if (c >= p.ws.meta[1]) return;  // (0 when cu_seqlens were rejected)
+  uint64_t* sbar = reinterpret_cast<uint64_t*>(sm + L::OFF_BAR);  // [0] operand copies, [1] Gram MMAs
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(sbar + 2);
+  if (tid == 0) {
+    mbar_init(sbar, 1);
+    mbar_init(sbar + 1, 1);
+    fence_mbar_init();
+  }
+  if ((tid >> 5) == 0) tmem_alloc(tslot, kCh);  // the Gram accumulators: 128 lanes x 64 columns
   const int4 rec = p.ws.chunks[c];
   const int i = rec.x, len = rec.z;
   const long long tok0 = rec.y, s0 = rec.w;
@@ -258,40 +286,53 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
     }
   }
 
-  // Gram products k^_t . k^_j and q^_t . k^_j: thread (tb, jb) takes t = tb + 16a, j = jb + 16b
+  // Gram products k^_t . k^_j and q^_t . k^_j on the tensor cores, from the split operands just
+  // written (three bf16 MMAs over the hi/lo pairs, as in the state kernel).  They come back from
+  // L2 into the conv table's space, dead once split, as [k^ hi | q^ hi | k^ lo | q^ lo]: k^ and
+  // q^ then read as one M = 128 operand and k^ alone as the N = 64 one.  TMEM lane r holds row r
+  // of [k^ k^T ; q^ k^T].
   {
-    const int tb = tid >> 4, jb = tid & 15;
-    float2 kk[4][4], qk[4][4];  // (even, odd channel) partial sums
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int bb = 0; bb < 4; ++bb) kk[a][bb] = qk[a][bb] = make_float2(0.f, 0.f);
-#pragma unroll 2
-    for (int c4 = 0; c4 < DK / 4; ++c4) {
-      float4 kt[4], qt[4], kj[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        kt[a] = *reinterpret_cast<const float4*>(sY + (tb + 16 * a) * L::YS + DK + 4 * c4);
-        qt[a] = *reinterpret_cast<const float4*>(sY + (tb + 16 * a) * L::YS + 4 * c4);
-        kj[a] = *reinterpret_cast<const float4*>(sY + (jb + 16 * a) * L::YS + DK + 4 * c4);
+    constexpr uint32_t BLK = kCh * DK * 2;
+    uint8_t* sOp = reinterpret_cast<uint8_t*>(sY);
+    const uint8_t* src = reinterpret_cast<const uint8_t*>(p.ws.kq) + (size_t(c) * p.Hk + kh) * kKqBlocks * BLK;
+    asm volatile("fence.proxy.async.global;" ::: "memory");  // this thread's operand stores, before the copies
+    tc_fence_before();
+    __syncthreads();  // every operand store fenced, every read of the conv table done
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    if (tid == 0) {
+      mbar_arrive_expect_tx(sbar, 4 * BLK);
+      bulk_load(sOp, src, BLK, sbar);                     // k^ hi
+      bulk_load(sOp + BLK, src + 2 * BLK, BLK, sbar);     // q^ hi
+      bulk_load(sOp + 2 * BLK, src + BLK, BLK, sbar);     // k^ lo
+      bulk_load(sOp + 3 * BLK, src + 3 * BLK, BLK, sbar); // q^ lo
+      if (mbar_wait_bounded(sbar, 0)) {
+        tc_fence_after();
+        const uint32_t a0 = smem_addr(sOp);
+        umma_split3<DK / 16>(tmem, a0, a0 + 2 * BLK, a0, a0 + 2 * BLK, (DK / 8) * 128, umma_idesc_bf16(2 * kCh, kCh),
+                             false);
+        umma_commit(sbar + 1);
       }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int bb = 0; bb <= a; ++bb) {  // blocks with bb > a lie above the diagonal: unused
-          kk[a][bb] = __ffma2_rn(make_float2(kt[a].x, kt[a].y), make_float2(kj[bb].x, kj[bb].y), kk[a][bb]);
-          kk[a][bb] = __ffma2_rn(make_float2(kt[a].z, kt[a].w), make_float2(kj[bb].z, kj[bb].w), kk[a][bb]);
-          qk[a][bb] = __ffma2_rn(make_float2(qt[a].x, qt[a].y), make_float2(kj[bb].x, kj[bb].y), qk[a][bb]);
-          qk[a][bb] = __ffma2_rn(make_float2(qt[a].z, qt[a].w), make_float2(kj[bb].z, kj[bb].w), qk[a][bb]);
-        }
     }
-#pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int bb = 0; bb < 4; ++bb) {
-        sm[L::OFF_KK + (tb + 16 * a) * kAS + jb + 16 * bb] = kk[a][bb].x + kk[a][bb].y;
-        sm[L::OFF_QK + (tb + 16 * a) * kAS + jb + 16 * bb] = qk[a][bb].x + qk[a][bb].y;
+    const bool ok = !__syncthreads_or(!mbar_wait_bounded(sbar + 1, 0));
+    tc_fence_after();
+    if (!ok) {
+      if (tid == 0) {
+        atomicOr(p.err, kDevErrTimeout);
+        (void)mbar_wait_bounded(sbar, 0);  // one more bounded wait for the copies in flight
       }
+    } else if (tid < 2 * kCh) {  // warps 0..3: thread = TMEM lane = row
+      float* dst = sm + ((tid < kCh) ? L::OFF_KK + tid * kAS : L::OFF_QK + (tid - kCh) * kAS);
+      const uint32_t lane_sel = uint32_t(32 * (tid >> 5)) << 16;
+#pragma unroll
+      for (int c0 = 0; c0 < kCh; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem + lane_sel + c0, v);
+#pragma unroll
+        for (int q = 0; q < 32; ++q) dst[c0 + q] = v[q];
+      }
+    }
+    tc_fence_before();
   }
   __syncthreads();  // the q|k table is dead from here: its space holds D, X and beta D (k.k)
 
@@ -456,6 +497,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
     }
     __syncthreads();
   }
+  tc_fence_after();
+  if ((tid >> 5) == 0) tmem_dealloc(*tslot, kCh);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -518,24 +561,6 @@ __device__ __forceinline__ bool epi_any(bool v) {
       : "r"(uint32_t(v))
       : "memory");
   return r != 0;
-}
-
-// One product of the chunk form as three bf16 MMA chains over hi/lo operand pairs (hi.hi, hi.lo,
-// lo.hi) of KSTEPS steps of K = 16 each.  Descriptors are formed once; a K step moves the start
-// address field by 256 bytes (two core matrices).
-template <int KSTEPS>
-__device__ __forceinline__ void umma_split3(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
-                                            uint32_t sbo, uint32_t idesc, bool accumulate) {
-  const uint64_t dah = umma_smem_desc(a_hi, 128, sbo), dal = umma_smem_desc(a_lo, 128, sbo);
-  const uint64_t dbh = umma_smem_desc(b_hi, 128, sbo), dbl = umma_smem_desc(b_lo, 128, sbo);
-#pragma unroll
-  for (int sp = 0; sp < 3; ++sp) {
-    const uint64_t da = (sp == 2) ? dal : dah;
-    const uint64_t db = (sp == 1) ? dbl : dbh;
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk)
-      umma_bf16(d, da + uint64_t(16 * kk), db + uint64_t(16 * kk), idesc, (accumulate || sp > 0 || kk > 0) ? 1u : 0u);
-  }
 }
 
 // The same with an MN-major B operand (the k^ blocks read as [c][t]): LBO is the byte step between
