@@ -62,12 +62,14 @@ def verify_bytes(d, out_bytes: int = 2) -> int:
 PREFILL_LENS = [8192] * 8  # prompts of the prefill measurement
 
 
-def prefill_mma_flops(n_chunks: int, Hv: int, dk: int, dv: int) -> int:
-    """bf16 tensor-core FLOPs the prefill state kernel issues: per (chunk, v-head, 64 state rows),
-    three MMAs (hi.hi, hi.lo, lo.hi) for each of S [k^|q^]^T (2 x 64 x 64 x dk), u = r W^T and
-    o = u MQ^T (64 x 64 x 64 each) and the state update (64 x dk x 64)."""
-    macs = 3 * (2 * 64 * 64 * dk + 2 * 64 * 64 * 64 + 64 * dk * 64)
-    return 2 * macs * n_chunks * Hv * (dv // 64)
+def prefill_mma_flops(n_chunks: int, Hk: int, Hv: int, dk: int, dv: int) -> int:
+    """bf16 tensor-core FLOPs one prefill call issues, three MMAs (hi.hi, hi.lo, lo.hi) per
+    product.  State kernel, per (chunk, v-head, 64 state rows): S [k^|q^]^T (2 x 64 x 64 x dk),
+    u = r W^T and o = u MQ^T (64 x 64 x 64 each) and the state update (64 x dk x 64).  Chunk
+    kernel, per (chunk, q/k head): the Gram products [k^; q^] k^T (128 x 64 x dk)."""
+    state = 3 * (2 * 64 * 64 * dk + 2 * 64 * 64 * 64 + 64 * dk * 64) * Hv * (dv // 64)
+    gram = 3 * (128 * 64 * dk) * Hk
+    return 2 * (state + gram) * n_chunks
 
 
 def measured_peak_tflops():
@@ -126,7 +128,7 @@ def run_prefill(args, world, dev, barrier, max_over_ranks):
     if gdn.gdn_device_status(clear=True):
         raise RuntimeError("device status flags after the prefill calls")
     chunks = sum((L + 63) // 64 for L in lens)
-    tf = prefill_mma_flops(chunks, d.Hv, d.dk, d.dv) / (ms * 1e-3) / 1e12
+    tf = prefill_mma_flops(chunks, d.Hk, d.Hv, d.dk, d.dv) / (ms * 1e-3) / 1e12
     peak, kind = measured_peak_tflops()
     res = {"value": world * N / (ms * 1e-3), "unit": "tokens/s", "ms_per_call": ms, "calls": n,
            "gpu_launches": 3 * n,
@@ -134,7 +136,8 @@ def run_prefill(args, world, dev, barrier, max_over_ranks):
                        "bf16 inputs and outputs, f32 state, in place",
            "tensor": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
                       "peak_source": f"{kind} (MEASURED_PEAKS.json bf16_tflops)",
-                      "what": "bf16 MMA FLOPs of the state kernel over the whole call (all three kernels)"},
+                      "what": "bf16 MMA FLOPs of the state and chunk kernels over the whole call "
+                              "(all three kernels)"},
            "what": "gdn_prefill per call: cu_seqlens check, per-chunk q/k kernel, tensor-core state pass"}
     del ws, out, x
     torch.cuda.empty_cache()
