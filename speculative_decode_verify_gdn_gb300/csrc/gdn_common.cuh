@@ -86,6 +86,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// After a wait on `bar` gave up (the device status word records it): keep waiting in bounded
+// slices, up to kDrainSlices more limits, for the transfers the CTA still has in flight on that
+// barrier (bulk copies, tensor-core groups, a cluster peer's asynchronous stores), so that it does
+// not exit while one of them can still write its shared or tensor memory.  A transfer between
+// valid, host-checked buffers completes within microseconds, so the slices run out only on a
+// device that is already failing.  True once the phase has completed.
+constexpr int kDrainSlices = 8;
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
+  for (int i = 0; i < kDrainSlices; ++i)
+    if (mbar_wait_bounded(bar, parity)) return true;
+  return false;
+}
+
 // ---------------------------------------------------------------- bulk async copies (TMA, linear)
 // global -> shared, completion counted on an mbarrier (bytes and addresses 16-byte aligned).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {

@@ -120,10 +120,11 @@ struct ChunkLayout {
   static constexpr int R_FLOATS = (Y_FLOATS > 2 * MAT) ? Y_FLOATS : 2 * MAT;
   static constexpr int OFF_KK = R_FLOATS;                     // [64][65] k^_t . k^_j
   static constexpr int OFF_QK = OFF_KK + MAT;                 // [64][65] q^_t . k^_j
-  static constexpr int OFF_BG = OFF_QK + MAT;                 // beta[64], G[64] (sum of log g), Gamma[64]
+  static constexpr int OFF_BG = OFF_QK + MAT;                 // beta[64], g[64], Gamma[64]
   static constexpr int OFF_Y2 = OFF_BG + 3 * kCh;             // [32][33] product temp of the inverse
   static constexpr int OFF_AB = OFF_Y2 + 32 * 33;             // a, b of the first kAbHeads v-heads [e][2][64]
-  static constexpr int OFF_BAR = (OFF_AB + kAbHeads * 2 * kCh + 1) & ~1;  // 2 mbarriers, the TMEM slot
+  static constexpr int OFF_QKD = OFF_AB + kAbHeads * 2 * kCh; // q^_t . k^_t in f32 [64]
+  static constexpr int OFF_BAR = (OFF_QKD + kCh + 1) & ~1;    // 2 mbarriers, the TMEM slot
   static constexpr int FLOATS = OFF_BAR + 6;
   static_assert(4 * kCh * DK * 2 <= R_FLOATS * 4, "the split q|k operands fit in the conv table's space");
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
@@ -260,6 +261,22 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   }
   __syncthreads();
 
+  // q^_t . k^_t in f32 from the normalised table: the diagonal of MQ.  Where a token's decay is 0
+  // its output is this one product times beta v, and a three-pass bf16 product's absolute error
+  // (about 2^-21 here) would be a large part of it when q^ and k^ are nearly orthogonal.
+  float* sQKd = sm + L::OFF_QKD;
+  {
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int t = warp; t < kCh; t += kThreads / 32) {
+      const float* row = sY + t * L::YS;
+      float acc = 0.f;
+#pragma unroll
+      for (int e = 0; e < DK / 32; ++e) acc = fmaf(row[lane + 32 * e], row[DK + lane + 32 * e], acc);
+      acc = warp_sum(acc);
+      if (lane == 0) sQKd[t] = acc;
+    }
+  }
+
   // normalised k^ and q^ to the workspace as bf16 hi/lo MMA operands (K-major core-matrix
   // layout, [t][c] with K = DK): k^ hi, k^ lo, q^ hi, q^ lo.  The state kernel also reads the k^
   // blocks as the MN-major operand [c][t] of its state update.  Eight consecutive threads fill
@@ -300,6 +317,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
     __syncthreads();  // every operand store fenced, every read of the conv table done
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    bool issued = false;  // (thread 0: the Gram MMAs were issued)
     if (tid == 0) {
       mbar_arrive_expect_tx(sbar, 4 * BLK);
       bulk_load(sOp, src, BLK, sbar);                     // k^ hi
@@ -312,14 +330,16 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
         umma_split3<DK / 16>(tmem, a0, a0 + 2 * BLK, a0, a0 + 2 * BLK, (DK / 8) * 128, umma_idesc_bf16(2 * kCh, kCh),
                              false);
         umma_commit(sbar + 1);
+        issued = true;
       }
     }
     const bool ok = !__syncthreads_or(!mbar_wait_bounded(sbar + 1, 0));
     tc_fence_after();
     if (!ok) {
-      if (tid == 0) {
+      if (tid == 0) {  // the copies and MMAs in flight finish before the TMEM is freed and the CTA exits
         atomicOr(p.err, kDevErrTimeout);
-        (void)mbar_wait_bounded(sbar, 0);  // one more bounded wait for the copies in flight
+        (void)mbar_drain(sbar, 0);
+        if (issued) (void)mbar_drain(sbar + 1, 0);
       }
     } else if (tid < 2 * kCh) {  // warps 0..3: thread = TMEM lane = row
       float* dst = sm + ((tid < kCh) ? L::OFF_KK + tid * kAS : L::OFF_QK + (tid - kCh) * kAS);
@@ -339,14 +359,13 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   float* sD = sm + L::OFF_D;  // D[t][j] (j <= t), later X = (I + beta D o KK)^-1
   float* sL = sm + L::OFF_L;
   float* sBeta = sm + L::OFF_BG;
-  float* sG = sBeta + kCh;  // log g, then its running sum G
+  float* sG = sBeta + kCh;  // g
   float* sGam = sG + kCh;
   for (int e = 0; e < r; ++e) {
     const int h = kh * r + e;
-    // a3 for this v-head (padding tokens: beta = 0, g = 1, so they change nothing); log g =
-    // softplus(a + dt_bias) A is kept, and G_t = sum_{m<=t} log g_m
+    // a3 for this v-head (padding tokens: beta = 0, g = 1, so they change nothing)
     if (tid < kCh) {
-      float beta = 0.f, lg = 0.f;
+      float beta = 0.f, g = 1.f;
       if (tid < len) {
         float av, bv;
         if (e < kAbHeads) {
@@ -359,40 +378,40 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
         }
         const float A = -expf(p.A_log[h]);
         const float z = av + p.dt_bias[h];
-        lg = ((z > 20.f) ? z : log1pf(expf(z))) * A;
+        g = expf(((z > 20.f) ? z : log1pf(expf(z))) * A);
         beta = gate_beta(bv);
       }
       sBeta[tid] = beta;
-      sG[tid] = lg;
+      sG[tid] = g;
     }
     __syncthreads();
-    if (tid < 32) {  // inclusive scan of log g over the chunk, two tokens per lane
-      const float v0 = sG[2 * tid], v1 = sG[2 * tid + 1];
-      float run = v0 + v1;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float n = __shfl_up_sync(0xffffffffu, run, o);
-        if (tid >= o) run += n;
+    // decay products D[t][j] = prod_{j<m<=t} g_m, a running product down each column (thread j),
+    // zeros above the diagonal (the blocked inverse relies on them); Gamma_t = prod_{m<=t} g_m
+    // (thread 64).  Every factor is in [0, 1]: nothing overflows, nothing cancels (a difference
+    // of running sums of log g would lose digits once those sums are large, and gives NaN after
+    // a token with g = 0), and a product that underflows is below anything it is added to.
+    if (tid < kCh) {
+      const int j = tid;
+      float d = 1.f;
+#pragma unroll 8
+      for (int t = 0; t < kCh; ++t) {
+        if (t > j) d *= sG[t];
+        sD[t * kAS + j] = (t < j) ? 0.f : d;
       }
-      __syncwarp();
-      sG[2 * tid] = run - v1;
-      sG[2 * tid + 1] = run;
+    } else if (tid == kCh) {
+      float gam = 1.f;
+#pragma unroll 8
+      for (int t = 0; t < kCh; ++t) {
+        gam *= sG[t];
+        sGam[t] = gam;
+      }
     }
-    __syncthreads();
-    // decay products D[t][j] = prod_{j<m<=t} g_m = exp(G_t - G_j) on and below the diagonal,
-    // zeros above it (the blocked inverse relies on them); Gamma_t = exp(G_t).  The exponent is
-    // never positive, where the hardware exp2 path (__expf) is within a few ulps: far inside the
-    // 2^-16 of the hi/lo MMA products these entries feed.
-    for (int idx = tid; idx < kCh * kCh; idx += kThreads) {
-      const int t = idx / kCh, j = idx % kCh;
-      sD[t * kAS + j] = (j <= t) ? __expf(sG[t] - sG[j]) : 0.f;
-    }
-    if (tid < kCh) sGam[tid] = expf(sG[tid]);
     __syncthreads();
     // per v-head operands: W hi, W lo, MQ hi, MQ lo, each [t][j] (K = 64), zero above the diagonal
     uint8_t* wq = reinterpret_cast<uint8_t*>(p.ws.wm) + (size_t(c) * p.Hv + h) * (4 * kCh * kCh * 2);
     float* gd = p.ws.gd + (size_t(c) * p.Hv + h) * (2 * kCh);
-    // beta_t D (k.k) strictly below the diagonal; MQ = D (q.k) on and below it; Gamma, d
+    // beta_t D (k.k) strictly below the diagonal; MQ = D (q.k) on and below it (D = 1 on the
+    // diagonal, where q.k is the f32 product); Gamma, d
     for (int idx = tid; idx < kCh * (kCh / 8); idx += kThreads) {
       const int cm = idx >> 3, r8 = idx & 7;
       const int t = (cm >> 3) * 8 + r8, jb = cm & 7;
@@ -401,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       for (int q = 0; q < 8; ++q) {
         const int j = 8 * jb + q;
         if (j < t) sL[t * kAS + j] = sBeta[t] * sD[t * kAS + j] * sm[L::OFF_KK + t * kAS + j];
-        v[q] = (j <= t) ? sD[t * kAS + j] * sm[L::OFF_QK + t * kAS + j] : 0.f;
+        v[q] = (j < t) ? sD[t * kAS + j] * sm[L::OFF_QK + t * kAS + j] : ((j == t) ? sQKd[t] : 0.f);
       }
       uint4 hi, lo;
       split8(v, hi, lo);
@@ -1058,10 +1077,10 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
   failed = __syncthreads_or(failed) != 0;
 
   if (failed) {
-    if (tid == kIssuer) {  // one more bounded wait for every copy and MMA group still in flight
+    if (tid == kIssuer) {  // every copy and MMA group still in flight lands before TMEM is freed
       atomicOr(p.err, kDevErrTimeout);
       for (int q = 0; q < kNumBars; ++q)
-        if (armed[q] > 0) (void)mbar_wait_bounded(bar + q, uint32_t(armed[q] - 1) & 1u);
+        if (armed[q] > 0) (void)mbar_drain(bar + q, uint32_t(armed[q] - 1) & 1u);
     }
   } else {
     // final state from TMEM

@@ -567,7 +567,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   if (!ok) {
     if (lane == 0) {
       atomicOr(p.err, kDevErrTimeout);
-      (void)mbar_wait_bounded(bar, 0);  // give the copies in flight one more bounded wait
+      (void)mbar_drain(bar, 0);  // the copies in flight land before this warp moves on
     }
     __syncwarp();
     if constexpr (!kGated) return;
@@ -688,7 +688,10 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   // into its shared memory, so none exits while a peer still writes to it.
   auto gated_finish = [&]() {
     const bool got = mbar_wait_bounded(bar_sq, 0);
-    if (!got && lane == 0) atomicOr(p.err, kDevErrTimeout);
+    if (!got) {  // (the peers' pushes still land before this CTA can exit)
+      if (lane == 0) atomicOr(p.err, kDevErrTimeout);
+      (void)mbar_drain(bar_sq, 0);
+    }
     if (ok && got) {
       // lane (m, cg) adds the partials of warps m, m + 4, ...; the xor over the m bits completes
       const float2* sSq = reinterpret_cast<const float2*>(sm + L::OFF_SQ);

@@ -2,16 +2,16 @@
 against the oracle's verify step followed by its gated_rms_norm, and its states against
 the plain verify step.
 
-Output tolerance: per (b, t, v-head) vector, max_i |y_i - y_ref_i| is bounded by OUT_TOL
-times the vector's scale max_i |o_ref_i| * rsqrt(mean o_ref^2 + eps) * max_i |w_i SiLU(z_i)|
-(the verify output's own bound carried through the norm; bf16 outputs add 2^-8).
+Output tolerance: the verify outputs' own, per (b, t, v-head) vector
+max_i |y_i - y_ref_i| / max_i |y_ref_i| <= 2e-3 (f32 outputs; bf16 outputs add 2^-8), with
+y_ref = the oracle's gated norm of the oracle's verify output.
 """
 import numpy as np
 import pytest
 import torch
 
 from oracle import gdn_oracle as O
-from parity_util import OUT_TOL, OUT_TOL_BF16, STATE_TOL, oracle_round, state_rel_err
+from parity_util import OUT_TOL, OUT_TOL_BF16, STATE_TOL, oracle_round, out_rel_err, state_rel_err
 from speculative_decode_verify_gdn_gb300 import gdn
 from speculative_decode_verify_gdn_gb300.build import build_library
 from speculative_decode_verify_gdn_gb300.runtime import GdnLayerState
@@ -32,14 +32,9 @@ def _lib():
 
 
 def _gated_err(y, o_ref, z_bits, w, eps):
-    zf = bf16_bits_to_f32(z_bits).astype(np.float64)
-    o_ref = np.asarray(o_ref, np.float64)
-    y_ref = O.gated_rms_norm(o_ref, zf, w, eps)
-    inv = 1.0 / np.sqrt(np.mean(o_ref * o_ref, axis=-1) + eps)
-    gate = np.abs(np.asarray(w, np.float64) * O.silu(zf))
-    scale = np.max(np.abs(o_ref), axis=-1) * inv * np.max(gate, axis=-1)
-    num = np.max(np.abs(np.asarray(y, np.float64) - y_ref), axis=-1)
-    return float(np.max(num / np.maximum(scale, 1e-30)))
+    """Per (b, t, v-head) vector: max |y - y_ref| / max |y_ref|, the plain outputs' metric."""
+    y_ref = O.gated_rms_norm(np.asarray(o_ref, np.float64), bf16_bits_to_f32(z_bits).astype(np.float64), w, eps)
+    return out_rel_err(y, y_ref)
 
 
 def _run_gated(d, lay, rnd, z_bits, w, eps, out_f32=True, q_scale=1.0):

@@ -14,8 +14,8 @@ from parity_util import OUT_TOL, OUT_TOL_BF16, STATE_TOL, out_rel_err, state_rel
 from speculative_decode_verify_gdn_gb300 import gdn
 from speculative_decode_verify_gdn_gb300.build import build_library
 from speculative_decode_verify_gdn_gb300.runtime import GdnLayerState
-from speculative_decode_verify_gdn_gb300.synth import (WORKLOADS, Dims, Dists, Gen, Round, bf16_bits_to_f32,
-                                                        make_layer, make_prompts)
+from speculative_decode_verify_gdn_gb300.synth import (WORKLOADS, Dims, Dists, Gen, Layer, Prompts, Round,
+                                                        bf16_bits_to_f32, make_layer, make_prompts)
 
 pytestmark = pytest.mark.gpu
 
@@ -170,3 +170,35 @@ def test_many_short_prompts():
     lens = [int(v) for v in g0.integers((1500,), 0, 5)]
     d, lay, pr = _problem(1210, lens, Hk=1, Hv=2, dk=64, dv=64)
     _check(_run(d, lay, pr), _oracle(d, lay, pr))
+
+
+def _head_group(d, lay, pr, i, kh):
+    """q/k head kh of prompt i as a problem of its own (Hk = 1 and the kh-th group of r v-heads):
+    the channels, taps, gates, history and state that those outputs depend on, nothing else."""
+    r = d.Hv // d.Hk
+    heads = np.arange(kh * r, kh * r + r)
+    ch = np.concatenate([kh * d.dk + np.arange(d.dk), d.Hk * d.dk + kh * d.dk + np.arange(d.dk),
+                         2 * d.Hk * d.dk + (heads[:, None] * d.dv + np.arange(d.dv)).ravel()])
+    s, e = int(pr.cu[i]), int(pr.cu[i + 1])
+    d1 = Dims(B=1, K=1, Hk=1, Hv=r, dk=d.dk, dv=d.dv)
+    lay1 = Layer(conv_w=lay.conv_w[ch], A_log=lay.A_log[heads], dt_bias=lay.dt_bias[heads],
+                 conv_state=lay.conv_state[i:i + 1][:, :, ch], state=lay.state[i:i + 1, heads])
+    pr1 = Prompts(np.array([0, e - s], np.int32), pr.x[s:e][:, ch], pr.a[s:e][:, heads], pr.b[s:e][:, heads])
+    return d1, lay1, pr1, heads, ch, slice(s, e)
+
+
+def test_8192_token_prompt_at_the_serving_shape_sampled_heads():
+    """A prompt of 8192 tokens (128 chunks, the benchmark's prompt length) and a short one at
+    Hk=16, Hv=32, dk=dv=128, every head on the GPU; sampled q/k head groups against the oracle
+    run on those heads alone: every output token of the group, its final state after 128
+    chunks and its conv history."""
+    w = WORKLOADS["serve16"]
+    d, lay, pr = _problem(1212, [8192, 100], Hk=w.dims.Hk, Hv=w.dims.Hv, dk=w.dims.dk, dv=w.dims.dv,
+                          dists=w.dists)
+    out, st, cs = _run(d, lay, pr, out_f32=True)
+    for i, kh in [(0, 0), (0, 9), (0, 15), (1, 4)]:
+        d1, lay1, pr1, heads, ch, rows = _head_group(d, lay, pr, i, kh)
+        ref = _oracle(d1, lay1, pr1)
+        assert out_rel_err(out[rows][:, heads], ref["out"]) <= OUT_TOL
+        assert state_rel_err(st[i, heads], ref["state_out"][0]) <= STATE_TOL
+        np.testing.assert_array_equal(cs[i][:, ch], ref["conv_state_out"][0])
