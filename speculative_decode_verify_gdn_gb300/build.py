@@ -78,18 +78,31 @@ def _code_only(text: str) -> str:
     return " ".join("".join(out).split())
 
 
-def kernel_source_digest() -> str:
-    """Hash of the CUDA sources without their comments, and of the flags: identifies the
-    kernels a profile was taken on, and stays put when only commentary changes."""
+def _code_digest(files) -> str:
     h = hashlib.sha256()
-    files = sources() + sorted(os.path.join(CSRC_DIR, f) for f in os.listdir(CSRC_DIR)
-                               if f.endswith((".cuh", ".h"))) + [HEADER]
     for f in files:
         h.update(os.path.basename(f).encode())
         with open(f, encoding="utf-8") as fh:
             h.update(_code_only(fh.read()).encode())
     h.update(" ".join(NVCC_FLAGS).encode())
     return h.hexdigest()[:16]
+
+
+def kernel_source_digest() -> str:
+    """Hash of all CUDA sources without their comments, and of the flags: identifies the
+    kernels a profile was taken on, and stays put when only commentary changes."""
+    return _code_digest(sources() + sorted(os.path.join(CSRC_DIR, f) for f in os.listdir(CSRC_DIR)
+                                           if f.endswith((".cuh", ".h"))) + [HEADER])
+
+
+# the translation unit of the verify kernels and everything it includes
+VERIFY_SOURCES = ("gdn_verify.cu", "gdn_common.cuh", "gdn_kernels.h")
+
+
+def verify_kernel_digest() -> str:
+    """The same hash over the verify kernels' sources only (gdn_verify.cu, the headers it
+    includes, and gdn.h): a profile of those kernels stays valid across edits elsewhere."""
+    return _code_digest([os.path.join(CSRC_DIR, f) for f in VERIFY_SOURCES] + [HEADER])
 
 
 def build_library(force: bool = False, verbose: bool = False) -> str:

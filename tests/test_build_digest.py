@@ -17,3 +17,16 @@ def test_digest_is_stable_and_short():
     d = build.kernel_source_digest()
     assert d == build.kernel_source_digest()
     assert len(d) == 16 and int(d, 16) >= 0
+
+
+def test_verify_digest_covers_exactly_the_verify_translation_unit():
+    """gdn_verify.cu includes gdn_common.cuh and gdn_kernels.h (which include gdn.h) and nothing
+    else of this library, so those files are the ones its digest must cover."""
+    import os
+    import re
+    src = open(os.path.join(build.CSRC_DIR, "gdn_verify.cu")).read()
+    local = set(re.findall(r'#include "([^"]+)"', src))
+    assert local == {"gdn_common.cuh", "gdn_kernels.h"}
+    assert set(build.VERIFY_SOURCES) == {"gdn_verify.cu"} | local
+    d = build.verify_kernel_digest()
+    assert len(d) == 16 and d == build.verify_kernel_digest() and d != build.kernel_source_digest()
