@@ -208,12 +208,55 @@ __device__ __forceinline__ void conv_channel(const VerifyParams& p, int b, int c
   hout[2 * C] = h2;
 }
 
+// Conv + SiLU of the two adjacent channels c, c + 1 (c even) over a chain window: one 4-byte load
+// per token for both x values, 8-byte history, snapshot and history stores.  The outputs go to
+// dst[t * ystride], dst[t * ystride + 1] (shared memory) for t < K, zero for K <= t < 16.
+__device__ __forceinline__ void conv_channel_pair(const VerifyParams& p, int b, int c, float* dst, int ystride) {
+  const int C = p.C;
+  const int K = p.K;
+  const float4 wa = *reinterpret_cast<const float4*>(p.conv_w + size_t(c) * kConvW);
+  const float4 wb = *reinterpret_cast<const float4*>(p.conv_w + size_t(c + 1) * kConvW);
+  const float* hin = history_src(p, b, c, prev_accept(p, b, false));
+  float2 h0 = *reinterpret_cast<const float2*>(hin);
+  float2 h1 = *reinterpret_cast<const float2*>(hin + C);
+  float2 h2 = *reinterpret_cast<const float2*>(hin + 2 * C);
+  const uint32_t* xp = reinterpret_cast<const uint32_t*>(p.x + size_t(b) * K * C + c);
+  uint32_t xv[kKMax];
+#pragma unroll
+  for (int t = 0; t < kKMax; ++t) xv[t] = (t < K) ? xp[size_t(t) * (C / 2)] : 0u;
+  float2* ci = p.conv_inter ? reinterpret_cast<float2*>(p.conv_inter + size_t(b) * K * 3 * C + c) : nullptr;
+  const size_t row2 = size_t(C) / 2;  // one history row, in float2
+#pragma unroll
+  for (int t = 0; t < kKMax; ++t) {
+    float2 y = make_float2(0.f, 0.f);
+    if (t < K) {
+      const float x0 = bf16_to_f32(uint16_t(xv[t] & 0xFFFFu)), x1 = bf16_to_f32(uint16_t(xv[t] >> 16));
+      y.x = silu(fmaf(wa.w, x0, fmaf(wa.z, h2.x, fmaf(wa.y, h1.x, wa.x * h0.x))));
+      y.y = silu(fmaf(wb.w, x1, fmaf(wb.z, h2.y, fmaf(wb.y, h1.y, wb.x * h0.y))));
+      h0 = h1;
+      h1 = h2;
+      h2 = make_float2(x0, x1);
+      if (ci) {
+        ci[(3 * t + 0) * row2] = h0;
+        ci[(3 * t + 1) * row2] = h1;
+        ci[(3 * t + 2) * row2] = h2;
+      }
+    }
+    *reinterpret_cast<float2*>(dst + t * ystride) = y;
+  }
+  float2* hout = reinterpret_cast<float2*>(p.conv_state_out + size_t(b) * 3 * C + c);
+  hout[0] = h0;
+  hout[row2] = h1;
+  hout[2 * row2] = h2;
+}
+
 // ------------------------------------------------------------------------------------------
 // Kernel 1: per (sequence, q/k head) prologue.
 template <int DK>
 struct PrologueLayout {
-  static constexpr int OFF_Y = 0;                           // raw conv outputs [32][DK] (k: 0..15, q: 16..31)
-  static constexpr int OFF_T = OFF_Y + kNCol * DK;          // normalised table [DK][32], swizzled as in global
+  static constexpr int YS = DK + 4;                         // conv row stride: rows 4 banks apart
+  static constexpr int OFF_Y = 0;                           // raw conv outputs [32][YS] (k: 0..15, q: 16..31)
+  static constexpr int OFF_T = OFF_Y + kNCol * YS;          // normalised table [DK][32], swizzled
   static constexpr int OFF_INV = OFF_T + DK * kNCol;        // 1 / sqrt(|y_n|^2 + eps) [32]
   static constexpr int OFF_KK = OFF_INV + kNCol;            // k^_t . k^_j  [16][17]
   static constexpr int OFF_KQ = OFF_KK + kKMax * kMStride;  // k^_j . q^_t  [16][17]
@@ -221,23 +264,8 @@ struct PrologueLayout {
   static constexpr int OFF_TREE = OFF_BG + 16 * 2 * kKMax;  // TreeTable (token trees only)
   static constexpr int FLOATS = OFF_TREE + int(sizeof(TreeTable) / 4);
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
-  static_assert(OFF_T % 4 == 0 && OFF_BG % 4 == 0, "float4 access");
+  static_assert(OFF_T % 4 == 0 && OFF_BG % 4 == 0 && YS % 4 == 0, "float4 access");
 };
-
-// Butterfly reduce-scatter of 32 values per lane across the warp: on return v[0] holds the warp
-// sum of value `lane` (five halvings, 31 shuffles per lane).
-__device__ __forceinline__ void warp_reduce_scatter(float (&v)[32], int lane) {
-#pragma unroll
-  for (int d = 16, half = 16; d >= 1; d >>= 1, half >>= 1) {
-    const bool upper = (lane & d) != 0;
-#pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, d);
-    }
-  }
-}
 
 template <int DK, bool kTree>
 __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const VerifyParams p) {
@@ -295,30 +323,41 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
     __syncthreads();
   }
 
-  // a1: conv of the head's q|k channels (thread cc < 2*DK owns one channel, its history, new
-  // history and snapshots; the snapshot stores leave from registers while the memory system is
-  // otherwise idle at the start of the step)
-  if (tid < 2 * DK) {
-    const int cc = tid;
-    const int c = (cc < DK) ? kh * DK + cc : p.Hk * DK + kh * DK + (cc - DK);
-    float y[kKMax];
-    conv_channel<kTree>(p, b, c, tree, y);
-    const int n0 = (cc < DK) ? kKMax : 0;  // q rows 16..31, k rows 0..15
-    const int col = cc % DK;
+  // a1: conv of the head's q|k channels (each channel's history, new history and snapshots have
+  // one owner thread; the snapshot stores leave from registers while the memory system is
+  // otherwise idle at the start of the step).  A chain window takes two adjacent channels per
+  // thread, a token tree one (its windows are gathered through the tree table)
+  if constexpr (kTree) {
+    if (tid < 2 * DK) {
+      const int cc = tid;
+      const int c = (cc < DK) ? kh * DK + cc : p.Hk * DK + kh * DK + (cc - DK);
+      float y[kKMax];
+      conv_channel<kTree>(p, b, c, tree, y);
+      const int n0 = (cc < DK) ? kKMax : 0;  // q rows 16..31, k rows 0..15
+      const int col = cc % DK;
 #pragma unroll
-    for (int t = 0; t < kKMax; ++t) sY[(n0 + t) * DK + col] = y[t];
+      for (int t = 0; t < kKMax; ++t) sY[(n0 + t) * L::YS + col] = y[t];
+    }
+  } else {
+    if (tid < DK) {
+      const int cc = 2 * tid;  // q channels 0..DK-1, then k channels (pairs never straddle them)
+      const int c = (cc < DK) ? kh * DK + cc : p.Hk * DK + kh * DK + (cc - DK);
+      const int n0 = (cc < DK) ? kKMax : 0;  // q rows 16..31, k rows 0..15
+      conv_channel_pair(p, b, c, sY + n0 * L::YS + cc % DK, L::YS);
+    }
   }
   __syncthreads();
 
   // a2: L2 norm of each of the 2K vectors (warp per vector, rows t >= K become zero), written
   // straight into the swizzled table; a3 for up to 16 v-heads alongside
+  float* kn = p.ws.kn + head * kKMax * DK;  // k^ token-major [16][DK], for the state updates
   for (int n = warp; n < kNCol; n += kWarps) {
     const int t = n % kKMax;
     float vals[DK / 32];
     float ss = 0.f;
 #pragma unroll
     for (int m = 0; m < DK / 32; ++m) {
-      vals[m] = sY[n * DK + lane + 32 * m];
+      vals[m] = sY[n * L::YS + lane + 32 * m];
       ss = fmaf(vals[m], vals[m], ss);
     }
     ss = warp_sum(ss);
@@ -328,55 +367,48 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
     for (int m = 0; m < DK / 32; ++m) {
       const int c = lane + 32 * m;
       sT[wt_idx(c, n)] = vals[m] * inv;
+      if (n < kKMax) kn[t * DK + c] = vals[m] * inv;
     }
   }
   gate_store(0);
   __syncthreads();
 
-  // tables for the state kernel: [DK][32] in plain column order (un-swizzled while copying) and
-  // the token-major k^ [16][DK]
+  // the [DK][32] table of k^ (columns 0..15) and q^ (16..31) for the state kernel, in plain column
+  // order: one 16-byte load per four columns, whose swizzle only permutes the four (logical column
+  // 4j + i sits at (4j ^ (s & ~3)) + (i ^ (s & 3)) with s = c & 31)
   {
     float* dst = p.ws.wt + head * DK * kNCol;
-    for (int f = tid; f < DK * kNCol; f += kThreads) dst[f] = sT[wt_idx(f / kNCol, f % kNCol)];
-    float* kn = p.ws.kn + head * kKMax * DK;
-    for (int f = tid; f < kKMax * DK; f += kThreads) kn[f] = sT[wt_idx(f % DK, f / DK)];
+    for (int f4 = tid; f4 < DK * (kNCol / 4); f4 += kThreads) {
+      const int c = f4 / (kNCol / 4), j = f4 % (kNCol / 4), x = c & 3;
+      const float4 v = *reinterpret_cast<const float4*>(sT + c * kNCol + ((4 * j) ^ (c & 28)));
+      const float w[4] = {v.x, v.y, v.z, v.w};
+      *reinterpret_cast<float4*>(dst + c * kNCol + 4 * j) = make_float4(w[x], w[1 ^ x], w[2 ^ x], w[3 ^ x]);
+    }
   }
 
-  // Gram products from the raw rows: warp w takes rows 4w..4w+3 of [k; q] against the 16 k
-  // rows, eight at a time; lanes split the channels, a butterfly reduce-scatter leaves one sum
-  // per lane
+  // Gram products from the raw rows: thread (n, j) takes row n of [k; q] against k rows j and
+  // j + 8 (a warp reads four n rows and sixteen k rows, all four banks apart), paired f32 FMAs
   {
-    constexpr int CPL = DK / 32;  // channels per lane
-    float rows[4][CPL];
-#pragma unroll
-    for (int m = 0; m < 4; ++m)
-#pragma unroll
-      for (int q = 0; q < CPL; ++q) rows[m][q] = sY[(4 * warp + m) * DK + CPL * lane + q];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float acc[32];
-#pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const int j = 8 * half + jj;
-        float kj[CPL];
-#pragma unroll
-        for (int q = 0; q < CPL; ++q) kj[q] = sY[j * DK + CPL * lane + q];
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          float a = 0.f;
-#pragma unroll
-          for (int q = 0; q < CPL; ++q) a = fmaf(rows[m][q], kj[q], a);
-          acc[m * 8 + jj] = a;
-        }
-      }
-      warp_reduce_scatter(acc, lane);  // acc[0] = sum of value `lane` = (row lane / 8, column lane % 8)
-      const int n = 4 * warp + lane / 8, j = 8 * half + lane % 8;
-      const float v = acc[0] * sInv[n] * sInv[j];
-      if (n < kKMax)
-        sKK[n * kMStride + j] = v;
-      else
-        sKQ[(n - kKMax) * kMStride + j] = v;
+    const int n = tid >> 3, j = tid & 7;
+    const float* yn = sY + n * L::YS;
+    const float* ya = sY + j * L::YS;
+    const float* yb = sY + (j + 8) * L::YS;
+    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll 8
+    for (int c = 0; c < DK; c += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(yn + c);
+      const float4 u = *reinterpret_cast<const float4*>(ya + c);
+      const float4 v = *reinterpret_cast<const float4*>(yb + c);
+      a0 = __ffma2_rn(make_float2(x.x, x.y), make_float2(u.x, u.y), a0);
+      a0 = __ffma2_rn(make_float2(x.z, x.w), make_float2(u.z, u.w), a0);
+      a1 = __ffma2_rn(make_float2(x.x, x.y), make_float2(v.x, v.y), a1);
+      a1 = __ffma2_rn(make_float2(x.z, x.w), make_float2(v.z, v.w), a1);
     }
+    const float sn = sInv[n];
+    const float v0 = (a0.x + a0.y) * sn * sInv[j], v1 = (a1.x + a1.y) * sn * sInv[j + 8];
+    float* dst = (n < kKMax) ? sKK + n * kMStride : sKQ + (n - kKMax) * kMStride;
+    dst[j] = v0;
+    dst[j + 8] = v1;
   }
   __syncthreads();
 
@@ -446,8 +478,9 @@ template <int DK, bool kGated = false>
 struct StreamLayout {
   static constexpr int PSTRIDE = kNCol + 4;                    // 16-byte rows
   static constexpr int RSTRIDE = kKMax + 1;
-  static constexpr int OFF_S0 = 0;                               // [32][DK]      bulk copy
-  static constexpr int OFF_WT = OFF_S0 + kRows * DK;             // [DK][32]      bulk copy
+  static constexpr int SSTRIDE = DK + 4;                         // S0 rows 4 banks apart
+  static constexpr int OFF_S0 = 0;                               // [32][SSTRIDE] bulk copy per row
+  static constexpr int OFF_WT = OFF_S0 + kRows * SSTRIDE;        // [DK][32]      bulk copy
   static constexpr int OFF_GATE = OFF_WT + DK * kNCol;           // gate block    bulk copy
   static constexpr int OFF_KN = OFF_GATE + kGateFloats;          // [16][DK] k^ token-major, bulk copy
   static constexpr int OFF_V = OFF_KN + kKMax * DK;              // [warp][16][4] v conv outputs
@@ -461,12 +494,13 @@ struct StreamLayout {
   static constexpr int OFF_BAR = (OFF_X + X_FLOATS + 1) & ~1;            // 8-byte aligned mbarrier(s)
   static constexpr int FLOATS = OFF_BAR + (kGated ? 4 : 2);              // gated: + the exchange mbarrier
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
-  static constexpr uint32_t S0_BYTES = kRows * DK * 4;
+  static constexpr uint32_t S0_ROW_BYTES = DK * 4;
+  static constexpr uint32_t S0_BYTES = kRows * S0_ROW_BYTES;
   static constexpr uint32_t WT_BYTES = DK * kNCol * 4;
   static constexpr uint32_t GATE_BYTES = kGateFloats * 4;
   static constexpr uint32_t KN_BYTES = kKMax * DK * 4;
   static_assert(OFF_SQ % 2 == 0, "gated exchange slots 8-byte aligned");
-  static_assert(S0_BYTES % 16 == 0 && WT_BYTES % 16 == 0 && GATE_BYTES % 16 == 0 && KN_BYTES % 16 == 0, "");
+  static_assert(S0_ROW_BYTES % 16 == 0 && (SSTRIDE * 4) % 16 == 0 && WT_BYTES % 16 == 0 && GATE_BYTES % 16 == 0 && KN_BYTES % 16 == 0, "");
   static_assert(OFF_WT % 4 == 0 && OFF_GATE % 4 == 0 && OFF_KN % 4 == 0 && OFF_P % 4 == 0,
                 "bulk destinations and float4 rows 16-byte aligned");
 };
@@ -510,17 +544,19 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   }
   if constexpr (kGated) cluster_arrive_relaxed();  // this CTA runs: the head's peers may write its smem later
   __syncthreads();  // the barrier is ready before any thread uses it
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES);
+  if (warp == 0) {
+    if (lane == 0) mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES);
     // S0: the previous final state, or (rollback applied on read) the accepted intermediate or
-    // the pre-window snapshot of the previous window
-    const int Lp = prev_accept(p, b, blockIdx.x == 0);
+    // the pre-window snapshot of the previous window; one row per lane, into rows padded by four
+    // banks so that the four rows a warp reads together in the products below do not conflict
+    const int Lp = prev_accept(p, b, blockIdx.x == 0 && lane == 0);
     const float* s0 = p.state_in + tile_off;
     if (Lp == 0)
       s0 = p.state_snap_prev + tile_off;
     else if (Lp > 0 && Lp < K)
       s0 = p.state_inter_prev + (size_t(b) * (K - 1) + (Lp - 1)) * size_t(p.Hv) * DV * DK + (size_t(h) * DV + r0) * DK;
-    bulk_load(sS0, s0, L::S0_BYTES, bar);
+    __syncwarp();  // (the expected byte count is set before any row can land)
+    bulk_load(sS0 + lane * L::SSTRIDE, s0 + size_t(lane) * DK, L::S0_ROW_BYTES, bar);
   }
   // gated: the lane's two z values of the epilogue, (token cg, row m of its warp) and eight tokens
   // later, and the row's norm weight, fetched now so that they have long arrived when used (the
@@ -587,6 +623,36 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   // gated: o of (row m, tokens cg and cg + 8), scaled by w SiLU(z) once its square is taken, and
   // the squares themselves
   float o_a = 0.f, o_b = 0.f, sq_a = 0.f, sq_b = 0.f;
+  // outputs o_t = q_scale Gamma_t Pq_t + sum_{j<=t} N[t][j] u_j: lane -> (row m, tokens cg, cg + 8).
+  // No state depends on them, so the plain and tree variants compute them after the state
+  // stream, off the path to the first store; the gated variant needs them inside the stream.
+  auto outputs = [&]() {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int t = cg + 8 * half;
+      if (t < K) {
+        float o = p.q_scale * gGam[t] * sP[(row0 + m) * L::PSTRIDE + kKMax + t];
+        for (int jj = 0; jj <= t; ++jj) o = fmaf(gN[t * kMStride + jj], sU[jj * kRowsPerWarp + m], o);
+        if constexpr (kGated) {
+          const float gz = nw * silu(bf16_to_f32(half ? z_b : z_a));
+          if (half == 0) {
+            sq_a = o * o;
+            o_a = o * gz;
+          } else {
+            sq_b = o * o;
+            o_b = o * gz;
+          }
+        } else {
+          const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
+          if (p.out_f32)
+            static_cast<float*>(p.out)[oi] = o;
+          else
+            static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(o);
+        }
+      }
+    }
+    __syncwarp();
+  };
   if (ok) {
   (void)mbar_try_wait(bar, 0);  // every lane observes the completed phase
 
@@ -594,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   // columns the right-hand side rhs_j = v_j - Gamma_j (S0 k^_j) right away
   {
     float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
-    const float* srow = sS0 + (row0 + m) * DK;
+    const float* srow = sS0 + (row0 + m) * L::SSTRIDE;
     const float* wcol = sWT + 4 * cg;
 #pragma unroll 4
     for (int c = 0; c < DK; c += 4) {
@@ -620,7 +686,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   }
   __syncwarp();
 
-  // forward substitution u_t = beta_t (rhs_t - sum_{j<t} M[t][j] u_j), lanes 0..3 (one row each)
+  // forward substitution u_t = beta_t (rhs_t - sum_{j<t} M[t][j] u_j), lanes 0..3 (one row each;
+  // a version that split each step's sum over all 32 lanes with shuffles took twice as long: the
+  // shuffles queue behind the shared-memory traffic of the neighbouring CTAs' state streams)
   if (lane < kRowsPerWarp) {
     const float* rh = sR + (row0 + lane) * L::RSTRIDE;
     float u[kKMax];
@@ -638,32 +706,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   }
   __syncwarp();
 
-  // outputs o_t = q_scale Gamma_t Pq_t + sum_{j<=t} N[t][j] u_j: lane -> (row m, tokens cg, cg + 8)
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int t = cg + 8 * half;
-    if (t < K) {
-      float o = p.q_scale * gGam[t] * sP[(row0 + m) * L::PSTRIDE + kKMax + t];
-      for (int jj = 0; jj <= t; ++jj) o = fmaf(gN[t * kMStride + jj], sU[jj * kRowsPerWarp + m], o);
-      if constexpr (kGated) {
-        const float gz = nw * silu(bf16_to_f32(half ? z_b : z_a));
-        if (half == 0) {
-          sq_a = o * o;
-          o_a = o * gz;
-        } else {
-          sq_b = o * o;
-          o_b = o * gz;
-        }
-      } else {
-        const size_t oi = (size_t(b) * K + t) * p.Hv * DV + size_t(h) * DV + r0 + row0 + m;
-        if (p.out_f32)
-          static_cast<float*>(p.out)[oi] = o;
-        else
-          static_cast<uint16_t*>(p.out)[oi] = f32_to_bf16(o);
-      }
-    }
-  }
-  __syncwarp();
+  if constexpr (kGated) outputs();
   }  // ok
 
   // gated: the exchange of the sums of o^2 over the warp's 4 rows (lanes m = 0..3 of one column
@@ -738,7 +781,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
 #pragma unroll
   for (int q = 0; q < F4; ++q) {
     rowq[q] = q * (32 / C4) + row_lane;
-    s[q] = *reinterpret_cast<const float4*>(sS0 + (row0 + rowq[q]) * DK + 4 * c4);
+    s[q] = *reinterpret_cast<const float4*>(sS0 + (row0 + rowq[q]) * L::SSTRIDE + 4 * c4);
   }
   const size_t inter_stride = size_t(p.Hv) * DV * DK;
   const size_t my_off = size_t(row0) * DK + 4 * c4;
@@ -769,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
         }
 #pragma unroll
         for (int q = 0; q < F4; ++q) {
-          const float4 s0v = *reinterpret_cast<const float4*>(sS0 + (row0 + rowq[q]) * DK + 4 * c4);
+          const float4 s0v = *reinterpret_cast<const float4*>(sS0 + (row0 + rowq[q]) * L::SSTRIDE + 4 * c4);
           s[q].x = fmaf(d, s0v.x, s[q].x);
           s[q].y = fmaf(d, s0v.y, s[q].y);
           s[q].z = fmaf(d, s0v.z, s[q].z);
@@ -780,9 +823,21 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
     const float g = gG[t];
     const float4 kv = *reinterpret_cast<const float4*>(sKn + t * DK + 4 * c4);
     float* dst = (t == K - 1) ? p.state_out + tile_off + my_off : inter + size_t(t) * inter_stride;
+    float uq[F4];  // u_t of the lane's rows: one 16-byte broadcast when a row spans the warp
+    if constexpr (C4 == 32) {
+      static_assert(F4 == kRowsPerWarp && L::OFF_U % 4 == 0, "the warp's four u values are one float4");
+      const float4 u4 = *reinterpret_cast<const float4*>(sU + t * kRowsPerWarp);
+      uq[0] = u4.x;
+      uq[1] = u4.y;
+      uq[2] = u4.z;
+      uq[3] = u4.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < F4; ++q) uq[q] = sU[t * kRowsPerWarp + rowq[q]];
+    }
 #pragma unroll
     for (int q = 0; q < F4; ++q) {
-      const float u = sU[t * kRowsPerWarp + rowq[q]];
+      const float u = uq[q];
       {  // s = g s + u k, two lanes of f32 per instruction
         const float2 gg = make_float2(g, g), uu = make_float2(u, u);
         const float2 lo = __ffma2_rn(uu, make_float2(kv.x, kv.y), __fmul2_rn(gg, make_float2(s[q].x, s[q].y)));
@@ -800,6 +855,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
       if (t == K / 2) gated_finish();
     }
   }
+  if constexpr (!kGated) outputs();
   }  // ok
 
   if constexpr (kGated) {
