@@ -132,32 +132,31 @@ __device__ __forceinline__ void build_tree(const VerifyParams& p, int b, TreeTab
 // Conv + SiLU of one channel over the window (a chain of K tokens, or a token tree when kTree);
 // writes the channel's K history snapshots and its new history (that after token / node K-1).
 // y[t] receives the outputs for t < K.  A token tree reads each node's window through the
-// table's indices, from `scratch` (3 + kKMax floats of shared memory) when given, else from a
-// thread-local array.
-template <bool kTree, bool kScratch = false>
+// table's indices: the three history values from registers, x_t from `scratch[t * sstride]`
+// (16 floats of shared memory per thread; a register array indexed at run time would live in
+// local memory).
+template <bool kTree>
 __device__ __forceinline__ void conv_channel(const VerifyParams& p, int b, int c, const TreeTable* tt,
-                                             float (&y)[kKMax], float* scratch = nullptr) {
+                                             float (&y)[kKMax], float* scratch = nullptr, int sstride = 1) {
   if constexpr (kTree) {
     const int C = p.C;
     const int K = p.K;
     const float4 w = *reinterpret_cast<const float4*>(p.conv_w + size_t(c) * kConvW);
     const float* hin = p.conv_state_in + size_t(b) * 3 * C + c;
-    float local_vals[kScratch ? 1 : 3 + kKMax];
-    float* vals = kScratch ? scratch : local_vals;  // [history rows 0..2, x_0 .. x_{K-1}]
-    vals[0] = hin[0];
-    vals[1] = hin[C];
-    vals[2] = hin[2 * C];
+    const float hv0 = hin[0], hv1 = hin[C], hv2 = hin[2 * C];
     const uint16_t* xp = p.x + size_t(b) * K * C + c;
 #pragma unroll
-    for (int t = 0; t < kKMax; ++t) vals[3 + t] = (t < K) ? bf16_to_f32(xp[size_t(t) * C]) : 0.f;
+    for (int t = 0; t < kKMax; ++t) scratch[t * sstride] = (t < K) ? bf16_to_f32(xp[size_t(t) * C]) : 0.f;
+    // value `idx` of [history rows 0, 1, 2, x_0 .. x_{K-1}]
+    auto val = [&](int idx) { return idx < 3 ? (idx == 0 ? hv0 : (idx == 1 ? hv1 : hv2)) : scratch[(idx - 3) * sstride]; };
     float* ci = p.conv_inter ? p.conv_inter + size_t(b) * K * 3 * C + c : nullptr;
     float n0 = 0.f, n1 = 0.f, n2 = 0.f;
 #pragma unroll
     for (int t = 0; t < kKMax; ++t) {
       y[t] = 0.f;
       if (t < K) {
-        const float w0 = vals[tt->src[t][0]], w1 = vals[tt->src[t][1]], w2 = vals[tt->src[t][2]];
-        const float xt = vals[3 + t];
+        const float w0 = val(tt->src[t][0]), w1 = val(tt->src[t][1]), w2 = val(tt->src[t][2]);
+        const float xt = scratch[t * sstride];
         y[t] = silu(fmaf(w.w, xt, fmaf(w.z, w2, fmaf(w.y, w1, w.x * w0))));
         n0 = w1;
         n1 = w2;
@@ -176,6 +175,8 @@ __device__ __forceinline__ void conv_channel(const VerifyParams& p, int b, int c
     return;
   }
   (void)tt;
+  (void)scratch;
+  (void)sstride;
   const int C = p.C;
   const int K = p.K;
   const float4 w = *reinterpret_cast<const float4*>(p.conv_w + size_t(c) * kConvW);
@@ -332,7 +333,8 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
       const int cc = tid;
       const int c = (cc < DK) ? kh * DK + cc : p.Hk * DK + kh * DK + (cc - DK);
       float y[kKMax];
-      conv_channel<kTree>(p, b, c, tree, y);
+      static_assert(kKMax * 2 * DK <= DK * kNCol, "16 scratch floats per conv thread fit in the table");
+      conv_channel<kTree>(p, b, c, tree, y, sT + cc, 2 * DK);  // (the table is written after the conv)
       const int n0 = (cc < DK) ? kKMax : 0;  // q rows 16..31, k rows 0..15
       const int col = cc % DK;
 #pragma unroll
@@ -588,7 +590,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
     float y[kKMax];
     // (a token tree's window values go through this row of the P table, which the warp only
     // fills after the load wait)
-    conv_channel<kTree, true>(p, b, 2 * p.Hk * DK + h * DV + r0 + i, tree, y, sm + L::OFF_P + i * L::PSTRIDE);
+    conv_channel<kTree>(p, b, 2 * p.Hk * DK + h * DV + r0 + i, tree, y, sm + L::OFF_P + i * L::PSTRIDE);
 #pragma unroll
     for (int t = 0; t < kKMax; ++t) sV[t * kRowsPerWarp + (lane - 4)] = y[t];
   }
@@ -800,13 +802,24 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
         float d = 1.f;
         for (int j = par; j >= 0; j = tree->parent[j]) {
           const float4 kj = *reinterpret_cast<const float4*>(sKn + j * DK + 4 * c4);
+          float uj[F4];  // u_j of the lane's rows (one 16-byte broadcast when a row spans the warp)
+          if constexpr (C4 == 32) {
+            const float4 u4 = *reinterpret_cast<const float4*>(sU + j * kRowsPerWarp);
+            uj[0] = u4.x;
+            uj[1] = u4.y;
+            uj[2] = u4.z;
+            uj[3] = u4.w;
+          } else {
+#pragma unroll
+            for (int q = 0; q < F4; ++q) uj[q] = sU[j * kRowsPerWarp + rowq[q]];
+          }
 #pragma unroll
           for (int q = 0; q < F4; ++q) {
-            const float uj = d * sU[j * kRowsPerWarp + rowq[q]];
-            s[q].x = fmaf(uj, kj.x, s[q].x);
-            s[q].y = fmaf(uj, kj.y, s[q].y);
-            s[q].z = fmaf(uj, kj.z, s[q].z);
-            s[q].w = fmaf(uj, kj.w, s[q].w);
+            const float du = d * uj[q];
+            s[q].x = fmaf(du, kj.x, s[q].x);
+            s[q].y = fmaf(du, kj.y, s[q].y);
+            s[q].z = fmaf(du, kj.z, s[q].z);
+            s[q].w = fmaf(du, kj.w, s[q].w);
           }
           d *= gG[j];
         }
