@@ -32,7 +32,7 @@ constexpr int kCh = kPrefillChunk;   // 64 tokens per chunk
 constexpr int kAS = kCh + 1;         // row stride of the chunk kernel's 64 x 64 shared tables
 constexpr int kTileRows = 64;        // state rows per state-kernel CTA (the MMA M)
 constexpr int kKqBlocks = 4;         // k^ hi, lo, q^ hi, lo per (chunk, q/k head)
-constexpr int kAbHeads = 8;          // v-heads per q/k head whose gate inputs the chunk kernel prefetches
+constexpr int kAbHeads = 4;          // v-heads per q/k head whose gate inputs the chunk kernel prefetches
 
 __device__ __forceinline__ float gate_beta(float b) { return 1.f / (1.f + expf(-b)); }
 
@@ -115,14 +115,15 @@ struct ChunkLayout {
   static constexpr int Y_FLOATS = kCh * YS;
   static constexpr int MAT = kCh * kAS;                       // one 64 x 65 matrix
   static constexpr int OFF_Y = 0;                             // [64][YS]: q (0..DK-1) | k (DK..2DK-1)
-  static constexpr int OFF_D = 0;                             // after the Gram products: D, then X
-  static constexpr int OFF_L = MAT;                           //   beta D (k.k), strictly lower
-  static constexpr int R_FLOATS = (Y_FLOATS > 2 * MAT) ? Y_FLOATS : 2 * MAT;
+  // after the Gram products, per v-head group g (two v-heads at a time): D, then X, at
+  // OFF_D + 2 g MAT, and beta D (k.k) strictly lower just after it
+  static constexpr int OFF_D = 0;
+  static constexpr int R_FLOATS = (Y_FLOATS > 4 * MAT) ? Y_FLOATS : 4 * MAT;
   static constexpr int OFF_KK = R_FLOATS;                     // [64][65] k^_t . k^_j
   static constexpr int OFF_QK = OFF_KK + MAT;                 // [64][65] q^_t . k^_j
-  static constexpr int OFF_BG = OFF_QK + MAT;                 // beta[64], g[64], Gamma[64]
-  static constexpr int OFF_Y2 = OFF_BG + 3 * kCh;             // [32][33] product temp of the inverse
-  static constexpr int OFF_AB = OFF_Y2 + 32 * 33;             // a, b of the first kAbHeads v-heads [e][2][64]
+  static constexpr int OFF_BG = OFF_QK + MAT;                 // per group: beta[64], g[64], Gamma[64]
+  static constexpr int OFF_Y2 = OFF_BG + 2 * 3 * kCh;         // per group: [32][33] product temp of the inverse
+  static constexpr int OFF_AB = OFF_Y2 + 2 * 32 * 33;         // a, b of the first kAbHeads v-heads [e][2][64]
   static constexpr int OFF_QKD = OFF_AB + kAbHeads * 2 * kCh; // q^_t . k^_t in f32 [64]
   static constexpr int OFF_BAR = (OFF_QKD + kCh + 1) & ~1;    // 2 mbarriers, the TMEM slot
   static constexpr int FLOATS = OFF_BAR + 6;
@@ -356,23 +357,31 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   }
   __syncthreads();  // the q|k table is dead from here: its space holds D, X and beta D (k.k)
 
-  float* sD = sm + L::OFF_D;  // D[t][j] (j <= t), later X = (I + beta D o KK)^-1
-  float* sL = sm + L::OFF_L;
-  float* sBeta = sm + L::OFF_BG;
+  // Per v-head work, two v-heads at a time: threads 0..127 take the even one, 128..255 the odd one,
+  // each half synchronising on a named barrier of its own (the phases below are chains of short
+  // steps, so two of them side by side fill the SM better than one after the other)
+  const int grp = tid >> 7, gt = tid & 127;
+  auto gsync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + grp) : "memory"); };
+  float* sD = sm + L::OFF_D + grp * 2 * L::MAT;  // D[t][j] (j <= t), later X = (I + beta D o KK)^-1
+  float* sL = sD + L::MAT;
+  float* sBeta = sm + L::OFF_BG + grp * 3 * kCh;
   float* sG = sBeta + kCh;  // g
   float* sGam = sG + kCh;
-  for (int e = 0; e < r; ++e) {
+  float* sY2 = sm + L::OFF_Y2 + grp * 32 * 33;
+  for (int e0 = 0; e0 < r; e0 += 2) {
+    const int e = e0 + grp;
+    if (e >= r) break;  // (an odd r leaves the second half idle on the last pair)
     const int h = kh * r + e;
     // a3 for this v-head (padding tokens: beta = 0, g = 1, so they change nothing)
-    if (tid < kCh) {
+    if (gt < kCh) {
       float beta = 0.f, g = 1.f;
-      if (tid < len) {
+      if (gt < len) {
         float av, bv;
         if (e < kAbHeads) {
-          av = sAB[(2 * e) * kCh + tid];
-          bv = sAB[(2 * e + 1) * kCh + tid];
+          av = sAB[(2 * e) * kCh + gt];
+          bv = sAB[(2 * e + 1) * kCh + gt];
         } else {
-          const size_t gi = size_t(tok0 + tid) * p.Hv + h;
+          const size_t gi = size_t(tok0 + gt) * p.Hv + h;
           av = bf16_to_f32(p.a[gi]);
           bv = bf16_to_f32(p.b[gi]);
         }
@@ -381,24 +390,24 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
         g = expf(((z > 20.f) ? z : log1pf(expf(z))) * A);
         beta = gate_beta(bv);
       }
-      sBeta[tid] = beta;
-      sG[tid] = g;
+      sBeta[gt] = beta;
+      sG[gt] = g;
     }
-    __syncthreads();
+    gsync();
     // decay products D[t][j] = prod_{j<m<=t} g_m, a running product down each column (thread j),
     // zeros above the diagonal (the blocked inverse relies on them); Gamma_t = prod_{m<=t} g_m
     // (thread 64).  Every factor is in [0, 1]: nothing overflows, nothing cancels (a difference
     // of running sums of log g would lose digits once those sums are large, and gives NaN after
     // a token with g = 0), and a product that underflows is below anything it is added to.
-    if (tid < kCh) {
-      const int j = tid;
+    if (gt < kCh) {
+      const int j = gt;
       float d = 1.f;
 #pragma unroll 8
       for (int t = 0; t < kCh; ++t) {
         if (t > j) d *= sG[t];
         sD[t * kAS + j] = (t < j) ? 0.f : d;
       }
-    } else if (tid == kCh) {
+    } else if (gt == kCh) {
       float gam = 1.f;
 #pragma unroll 8
       for (int t = 0; t < kCh; ++t) {
@@ -406,13 +415,13 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
         sGam[t] = gam;
       }
     }
-    __syncthreads();
+    gsync();
     // per v-head operands: W hi, W lo, MQ hi, MQ lo, each [t][j] (K = 64), zero above the diagonal
     uint8_t* wq = reinterpret_cast<uint8_t*>(p.ws.wm) + (size_t(c) * p.Hv + h) * (4 * kCh * kCh * 2);
     float* gd = p.ws.gd + (size_t(c) * p.Hv + h) * (2 * kCh);
     // beta_t D (k.k) strictly below the diagonal; MQ = D (q.k) on and below it (D = 1 on the
     // diagonal, where q.k is the f32 product); Gamma, d
-    for (int idx = tid; idx < kCh * (kCh / 8); idx += kThreads) {
+    for (int idx = gt; idx < kCh * (kCh / 8); idx += 128) {
       const int cm = idx >> 3, r8 = idx & 7;
       const int t = (cm >> 3) * 8 + r8, jb = cm & 7;
       float v[8];
@@ -428,17 +437,17 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       *reinterpret_cast<uint4*>(wq + 2 * (kCh * kCh * 2) + off) = hi;
       *reinterpret_cast<uint4*>(wq + 3 * (kCh * kCh * 2) + off) = lo;
     }
-    if (tid < kCh) {
-      gd[tid] = sGam[tid];
-      gd[kCh + tid] = sD[(kCh - 1) * kAS + tid];
+    if (gt < kCh) {
+      gd[gt] = sGam[gt];
+      gd[kCh + gt] = sD[(kCh - 1) * kAS + gt];
     }
-    __syncthreads();
+    gsync();
     // X = (I + L)^-1, blocked.  The four 16 x 16 diagonal blocks: one thread per column, forward
     // substitution unrolled in registers (x_t = 0 above the diagonal, 1 on it).  Then
     // X21 = -X22 (L21 X11) for the 16 x 16 and the 32 x 32 off-diagonal blocks, whose upper
     // triangles are zero.  X overwrites D.
-    if (tid < kCh) {
-      const int jb = tid & ~15, jj = tid & 15;
+    if (gt < kCh) {
+      const int jb = gt & ~15, jj = gt & 15;
       float x[16];
 #pragma unroll
       for (int t = 0; t < 16; ++t) {
@@ -448,58 +457,64 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
         x[t] = (t < jj) ? 0.f : ((t == jj) ? 1.f : -acc);
       }
 #pragma unroll
-      for (int t = 0; t < 16; ++t) sD[(jb + t) * kAS + tid] = x[t];
+      for (int t = 0; t < 16; ++t) sD[(jb + t) * kAS + gt] = x[t];
     }
-    __syncthreads();
-    float* sY2 = sm + L::OFF_Y2;
-    {  // 16 x 16 off-diagonal blocks of the two 32 x 32 blocks: thread = (block, row, 2 columns)
-      const int blk = tid >> 7, ii = (tid >> 3) & 15, jj = 2 * (tid & 7);
-      const int o = 32 * blk;
-      float y0 = 0.f, y1 = 0.f;
+    gsync();
+    {  // 16 x 16 off-diagonal blocks of the two 32 x 32 blocks: thread = (row, 2 columns), both blocks
+      const int ii = gt >> 3, jj = 2 * (gt & 7);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float l = sL[(o + 16 + ii) * kAS + o + k];
-        y0 = fmaf(l, sD[(o + k) * kAS + o + jj], y0);
-        y1 = fmaf(l, sD[(o + k) * kAS + o + jj + 1], y1);
-      }
-      sY2[(16 * blk + ii) * 33 + jj] = y0;
-      sY2[(16 * blk + ii) * 33 + jj + 1] = y1;
-      __syncthreads();
-      float x0 = 0.f, x1 = 0.f;
+      for (int blk = 0; blk < 2; ++blk) {
+        const int o = 32 * blk;
+        float y0 = 0.f, y1 = 0.f;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float xv = sD[(o + 16 + ii) * kAS + o + 16 + k];
-        x0 = fmaf(xv, sY2[(16 * blk + k) * 33 + jj], x0);
-        x1 = fmaf(xv, sY2[(16 * blk + k) * 33 + jj + 1], x1);
+        for (int k = 0; k < 16; ++k) {
+          const float l = sL[(o + 16 + ii) * kAS + o + k];
+          y0 = fmaf(l, sD[(o + k) * kAS + o + jj], y0);
+          y1 = fmaf(l, sD[(o + k) * kAS + o + jj + 1], y1);
+        }
+        sY2[(16 * blk + ii) * 33 + jj] = y0;
+        sY2[(16 * blk + ii) * 33 + jj + 1] = y1;
       }
-      sD[(o + 16 + ii) * kAS + o + jj] = -x0;
-      sD[(o + 16 + ii) * kAS + o + jj + 1] = -x1;
+      gsync();
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk) {
+        const int o = 32 * blk;
+        float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float xv = sD[(o + 16 + ii) * kAS + o + 16 + k];
+          x0 = fmaf(xv, sY2[(16 * blk + k) * 33 + jj], x0);
+          x1 = fmaf(xv, sY2[(16 * blk + k) * 33 + jj + 1], x1);
+        }
+        sD[(o + 16 + ii) * kAS + o + jj] = -x0;
+        sD[(o + 16 + ii) * kAS + o + jj + 1] = -x1;
+      }
     }
-    __syncthreads();
-    {  // the 32 x 32 off-diagonal block: thread = (row, 4 columns)
-      const int ii = tid >> 3, jj = 4 * (tid & 7);
-      float y[4] = {0.f, 0.f, 0.f, 0.f};
+    gsync();
+    {  // the 32 x 32 off-diagonal block: thread = (row, 8 columns)
+      const int ii = gt >> 2, jj = 8 * (gt & 3);
+      float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const float l = sL[(32 + ii) * kAS + k];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) y[q] = fmaf(l, sD[k * kAS + jj + q], y[q]);
+        for (int q = 0; q < 8; ++q) y[q] = fmaf(l, sD[k * kAS + jj + q], y[q]);
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sY2[ii * 33 + jj + q] = y[q];
-      __syncthreads();
-      float x[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int q = 0; q < 8; ++q) sY2[ii * 33 + jj + q] = y[q];
+      gsync();
+      float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const float xv = sD[(32 + ii) * kAS + 32 + k];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) x[q] = fmaf(xv, sY2[k * 33 + jj + q], x[q]);
+        for (int q = 0; q < 8; ++q) x[q] = fmaf(xv, sY2[k * 33 + jj + q], x[q]);
       }
 #pragma unroll
-      for (int q = 0; q < 4; ++q) sD[(32 + ii) * kAS + jj + q] = -x[q];
+      for (int q = 0; q < 8; ++q) sD[(32 + ii) * kAS + jj + q] = -x[q];
     }
-    __syncthreads();
-    for (int idx = tid; idx < kCh * (kCh / 8); idx += kThreads) {
+    gsync();
+    for (int idx = gt; idx < kCh * (kCh / 8); idx += 128) {
       const int cm = idx >> 3, r8 = idx & 7;
       const int t = (cm >> 3) * 8 + r8, jb = cm & 7;
       float v[8];
@@ -514,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
       *reinterpret_cast<uint4*>(wq + off) = hi;
       *reinterpret_cast<uint4*>(wq + (kCh * kCh * 2) + off) = lo;
     }
-    __syncthreads();
+    gsync();
   }
   tc_fence_after();
   if ((tid >> 5) == 0) tmem_dealloc(*tslot, kCh);

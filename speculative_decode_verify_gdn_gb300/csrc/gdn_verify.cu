@@ -65,8 +65,16 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Index of q^/k^ column `col` of channel `c` in the swizzled table.
-__device__ __forceinline__ int wt_idx(int c, int col) { return c * kNCol + (col ^ (c & 31)); }
+// Columns 4j .. 4j+3 of row c of the swizzled [DK][32] q^/k^ table (element (c, col) at
+// c * 32 + (col ^ (c & 31))) in plain order: one 16-byte load, whose swizzle only permutes the four
+// (logical column 4j + i sits at (4j ^ (s & ~3)) + (i ^ (s & 3)) with s = c & 31).
+__device__ __forceinline__ float4 unswizzled4(const float* sT, int c, int j) {
+  const int x = c & 3;
+  float4 v = *reinterpret_cast<const float4*>(sT + c * kNCol + ((4 * j) ^ (c & 28)));
+  if (x & 1) v = make_float4(v.y, v.x, v.w, v.z);
+  if (x & 2) v = make_float4(v.z, v.w, v.x, v.y);
+  return v;
+}
 
 // Accepted length of the previous window for sequence b, or -1 for a plain verify step (no
 // rollback applied on read).  Lengths outside 0..K, and 0 without a snapshot, read as K (the
@@ -251,6 +259,118 @@ __device__ __forceinline__ void conv_channel_pair(const VerifyParams& p, int b, 
   hout[2 * row2] = h2;
 }
 
+// a3 for one (v-head, token): beta = sigmoid(b), g = exp(softplus(a + dt_bias) * -exp(A_log)) with
+// the softplus clipped to the identity above 20.
+__device__ __forceinline__ void raw_gate(float a, float b, float A_log, float dt_bias, float& beta, float& g) {
+  const float A = -expf(A_log);
+  const float av = a + dt_bias;
+  const float sp = (av > 20.f) ? av : log1pf(expf(av));
+  g = expf(sp * A);
+  beta = 1.f / (1.f + expf(-b));
+}
+
+// a2 over the 2K q|k vectors of one q/k head, raw conv outputs in sY[32][ys] (k rows 0..15, q rows
+// 16..31): warp per vector, rows t >= K become zero.  Normalised values go to the swizzled
+// [DK][32] table sT and, for the k rows, token-major to kn[16][DK]; 1 / norm to sInv[32].
+template <int DK>
+__device__ __forceinline__ void qk_norms(const float* sY, int ys, float* sT, float* sInv, float* kn, int K,
+                                         float eps, int warp, int lane) {
+  for (int n = warp; n < kNCol; n += kWarps) {
+    const int t = n % kKMax;
+    float vals[DK / 32];
+    float ss = 0.f;
+#pragma unroll
+    for (int m = 0; m < DK / 32; ++m) {
+      vals[m] = sY[n * ys + lane + 32 * m];
+      ss = fmaf(vals[m], vals[m], ss);
+    }
+    ss = warp_sum(ss);
+    const float inv = (t < K) ? rsqrtf(ss + eps) : 0.f;
+    if (lane == 0) sInv[n] = inv;
+#pragma unroll
+    for (int m = 0; m < DK / 32; ++m) {
+      const int c = lane + 32 * m;
+      sT[c * kNCol + (n ^ (c & 31))] = vals[m] * inv;
+      if (n < kKMax) kn[t * DK + c] = vals[m] * inv;
+    }
+  }
+}
+
+// Gram products from the raw rows: thread (n, j) takes row n of [k; q] against k rows j and j + 8
+// (a warp reads four n rows and sixteen k rows, all four banks apart when ys = DK + 4), paired f32
+// FMAs; scaled by the two inverse norms into KK[t][j] = k^_t . k^_j and KQ[t][j] = k^_j . q^_t.
+template <int DK>
+__device__ __forceinline__ void qk_gram(const float* sY, int ys, const float* sInv, float* sKK, float* sKQ, int tid) {
+  const int n = tid >> 3, j = tid & 7;
+  const float* yn = sY + n * ys;
+  const float* ya = sY + j * ys;
+  const float* yb = sY + (j + 8) * ys;
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll 8
+  for (int c = 0; c < DK; c += 4) {
+    const float4 x = *reinterpret_cast<const float4*>(yn + c);
+    const float4 u = *reinterpret_cast<const float4*>(ya + c);
+    const float4 v = *reinterpret_cast<const float4*>(yb + c);
+    a0 = __ffma2_rn(make_float2(x.x, x.y), make_float2(u.x, u.y), a0);
+    a0 = __ffma2_rn(make_float2(x.z, x.w), make_float2(u.z, u.w), a0);
+    a1 = __ffma2_rn(make_float2(x.x, x.y), make_float2(v.x, v.y), a1);
+    a1 = __ffma2_rn(make_float2(x.z, x.w), make_float2(v.z, v.w), a1);
+  }
+  const float sn = sInv[n];
+  const float v0 = (a0.x + a0.y) * sn * sInv[j], v1 = (a1.x + a1.y) * sn * sInv[j + 8];
+  float* dst = (n < kKMax) ? sKK + n * kMStride : sKQ + (n - kKMax) * kMStride;
+  dst[j] = v0;
+  dst[j + 8] = v1;
+}
+
+// One v-head's gate block, thread (t, j) = (tid / 16, tid % 16) of 256: M = D o (k^.k^) strictly
+// lower, N = q_scale D o (k^.q^) lower, Gamma, beta, g, with D[t][j] = prod_{j<m<=t} g_m as a
+// masked product over registers (a token tree: over the path of t below j).  bg holds beta[16]
+// then g[16]; kk, kq are this thread's Gram entries.
+template <bool kTree>
+__device__ __forceinline__ void gate_block(const VerifyParams& p, const TreeTable* tree, const float* bg, float kk,
+                                           float kq, float* gate, int tid) {
+  const int t = tid >> 4, j = tid & 15;
+  float g[kKMax];
+#pragma unroll
+  for (int m = 0; m < kKMax; m += 4) {
+    const float4 v = *reinterpret_cast<const float4*>(bg + kKMax + m);
+    g[m] = v.x;
+    g[m + 1] = v.y;
+    g[m + 2] = v.z;
+    g[m + 3] = v.w;
+  }
+  // chain: j < t are the earlier tokens and the path below j is j+1..t; tree: j must lie on t's
+  // root-to-node path, and the nodes below it are t's path minus j's (same products, same order,
+  // so a chain-shaped tree gives the chain's numbers bit for bit)
+  bool below = j < t, on_path = j <= t;
+  unsigned down = 0;
+  int root = 0;
+  if constexpr (kTree) {
+    const unsigned pt = tree->path[t], pj = tree->path[j];
+    on_path = j <= t && ((pt >> j) & 1u);
+    below = on_path && j < t;
+    down = pt & ~pj;
+    root = __ffs(pt) - 1;
+  }
+  float d = 1.f;
+#pragma unroll
+  for (int m = 1; m < kKMax; ++m) {
+    const bool in = kTree ? ((down >> m) & 1u) : (m > j && m <= t);
+    d *= in ? g[m] : 1.f;
+  }
+  gate[t * kMStride + j] = below ? d * kk : 0.f;
+  gate[kGateOffN + t * kMStride + j] = on_path ? p.q_scale * d * kq : 0.f;
+  if (j == root) gate[kGateOffGam + t] = d * g[root];
+  if (tid < kKMax) {
+    gate[tid * kMStride + kKMax] = 0.f;
+    gate[kGateOffN + tid * kMStride + kKMax] = 0.f;
+    gate[kGateOffBeta + tid] = bg[tid];
+    gate[kGateOffG + tid] = bg[kKMax + tid];
+  }
+  if (tid < kGateFloats - (kGateOffGam + kKMax)) gate[kGateOffGam + kKMax + tid] = 0.f;
+}
+
 // ------------------------------------------------------------------------------------------
 // Kernel 1: per (sequence, q/k head) prologue.
 template <int DK>
@@ -306,13 +426,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
     const int hv = hv0 + (tid >> 4), t = tid & 15;
     if (hv < r) {
       float beta = 0.f, g = 1.f;
-      if (t < K) {
-        const float A = -expf(gA);
-        const float av = ga + gdt;
-        const float sp = (av > 20.f) ? av : log1pf(expf(av));
-        g = expf(sp * A);
-        beta = 1.f / (1.f + expf(-gb));
-      }
+      if (t < K) raw_gate(ga, gb, gA, gdt, beta, g);
       sBG[(hv - hv0) * 2 * kKMax + t] = beta;
       sBG[(hv - hv0) * 2 * kKMax + kKMax + t] = g;
     }
@@ -350,75 +464,28 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
   }
   __syncthreads();
 
-  // a2: L2 norm of each of the 2K vectors (warp per vector, rows t >= K become zero), written
-  // straight into the swizzled table; a3 for up to 16 v-heads alongside
-  float* kn = p.ws.kn + head * kKMax * DK;  // k^ token-major [16][DK], for the state updates
-  for (int n = warp; n < kNCol; n += kWarps) {
-    const int t = n % kKMax;
-    float vals[DK / 32];
-    float ss = 0.f;
-#pragma unroll
-    for (int m = 0; m < DK / 32; ++m) {
-      vals[m] = sY[n * L::YS + lane + 32 * m];
-      ss = fmaf(vals[m], vals[m], ss);
-    }
-    ss = warp_sum(ss);
-    const float inv = (t < K) ? rsqrtf(ss + p.l2_eps) : 0.f;
-    if (lane == 0) sInv[n] = inv;
-#pragma unroll
-    for (int m = 0; m < DK / 32; ++m) {
-      const int c = lane + 32 * m;
-      sT[wt_idx(c, n)] = vals[m] * inv;
-      if (n < kKMax) kn[t * DK + c] = vals[m] * inv;
-    }
-  }
+  // a2: L2 norm of each of the 2K vectors, straight into the swizzled table (and k^ token-major
+  // to the workspace, for the state updates); a3 for up to 16 v-heads alongside
+  qk_norms<DK>(sY, L::YS, sT, sInv, p.ws.kn + head * kKMax * DK, K, p.l2_eps, warp, lane);
   gate_store(0);
   __syncthreads();
 
   // the [DK][32] table of k^ (columns 0..15) and q^ (16..31) for the state kernel, in plain column
-  // order: one 16-byte load per four columns, whose swizzle only permutes the four (logical column
-  // 4j + i sits at (4j ^ (s & ~3)) + (i ^ (s & 3)) with s = c & 31)
+  // order
   {
     float* dst = p.ws.wt + head * DK * kNCol;
     for (int f4 = tid; f4 < DK * (kNCol / 4); f4 += kThreads) {
-      const int c = f4 / (kNCol / 4), j = f4 % (kNCol / 4), x = c & 3;
-      const float4 v = *reinterpret_cast<const float4*>(sT + c * kNCol + ((4 * j) ^ (c & 28)));
-      const float w[4] = {v.x, v.y, v.z, v.w};
-      *reinterpret_cast<float4*>(dst + c * kNCol + 4 * j) = make_float4(w[x], w[1 ^ x], w[2 ^ x], w[3 ^ x]);
+      const int c = f4 / (kNCol / 4), j = f4 % (kNCol / 4);
+      *reinterpret_cast<float4*>(dst + c * kNCol + 4 * j) = unswizzled4(sT, c, j);
     }
   }
 
-  // Gram products from the raw rows: thread (n, j) takes row n of [k; q] against k rows j and
-  // j + 8 (a warp reads four n rows and sixteen k rows, all four banks apart), paired f32 FMAs
-  {
-    const int n = tid >> 3, j = tid & 7;
-    const float* yn = sY + n * L::YS;
-    const float* ya = sY + j * L::YS;
-    const float* yb = sY + (j + 8) * L::YS;
-    float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
-#pragma unroll 8
-    for (int c = 0; c < DK; c += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(yn + c);
-      const float4 u = *reinterpret_cast<const float4*>(ya + c);
-      const float4 v = *reinterpret_cast<const float4*>(yb + c);
-      a0 = __ffma2_rn(make_float2(x.x, x.y), make_float2(u.x, u.y), a0);
-      a0 = __ffma2_rn(make_float2(x.z, x.w), make_float2(u.z, u.w), a0);
-      a1 = __ffma2_rn(make_float2(x.x, x.y), make_float2(v.x, v.y), a1);
-      a1 = __ffma2_rn(make_float2(x.z, x.w), make_float2(v.z, v.w), a1);
-    }
-    const float sn = sInv[n];
-    const float v0 = (a0.x + a0.y) * sn * sInv[j], v1 = (a1.x + a1.y) * sn * sInv[j + 8];
-    float* dst = (n < kKMax) ? sKK + n * kMStride : sKQ + (n - kKMax) * kMStride;
-    dst[j] = v0;
-    dst[j + 8] = v1;
-  }
+  qk_gram<DK>(sY, L::YS, sInv, sKK, sKQ, tid);
   __syncthreads();
 
-  // per-v-head gate blocks: M = D * (k^.k^) strictly lower, N = q_scale * D * (k^.q^) lower,
-  // Gamma, beta, g; D[t][j] = prod_{j<m<=t} g_m as a masked product over registers
-  const int t = tid >> 4, j = tid & 15;
-  const float kk = sKK[t * kMStride + j];
-  const float kq = sKQ[t * kMStride + j];
+  // per-v-head gate blocks
+  const float kk = sKK[(tid >> 4) * kMStride + (tid & 15)];
+  const float kq = sKQ[(tid >> 4) * kMStride + (tid & 15)];
   for (int hv0 = 0; hv0 < r; hv0 += 16) {
     if (hv0 > 0) {
       __syncthreads();
@@ -426,48 +493,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
       gate_store(hv0);
       __syncthreads();
     }
-    for (int hv = hv0; hv < min(r, hv0 + 16); ++hv) {
-      const float* bg = sBG + (hv - hv0) * 2 * kKMax;
-      float g[kKMax];
-#pragma unroll
-      for (int m = 0; m < kKMax; m += 4) {
-        const float4 v = *reinterpret_cast<const float4*>(bg + kKMax + m);
-        g[m] = v.x;
-        g[m + 1] = v.y;
-        g[m + 2] = v.z;
-        g[m + 3] = v.w;
-      }
-      // chain: j < t are the earlier tokens and the path below j is j+1..t; tree: j must lie on
-      // t's root-to-node path, and the nodes below it are t's path minus j's (same products,
-      // same order, so a chain-shaped tree gives the chain's numbers bit for bit)
-      bool below = j < t, on_path = j <= t;
-      unsigned down = 0;
-      int root = 0;
-      if constexpr (kTree) {
-        const unsigned pt = tree->path[t], pj = tree->path[j];
-        on_path = j <= t && ((pt >> j) & 1u);
-        below = on_path && j < t;
-        down = pt & ~pj;
-        root = __ffs(pt) - 1;
-      }
-      float d = 1.f;
-#pragma unroll
-      for (int m = 1; m < kKMax; ++m) {
-        const bool in = kTree ? ((down >> m) & 1u) : (m > j && m <= t);
-        d *= in ? g[m] : 1.f;
-      }
-      float* gate = p.ws.gate + (size_t(b) * p.Hv + kh * r + hv) * kGateFloats;
-      gate[t * kMStride + j] = below ? d * kk : 0.f;
-      gate[kGateOffN + t * kMStride + j] = on_path ? p.q_scale * d * kq : 0.f;
-      if (j == root) gate[kGateOffGam + t] = d * g[root];
-      if (tid < kKMax) {
-        gate[tid * kMStride + kKMax] = 0.f;
-        gate[kGateOffN + tid * kMStride + kKMax] = 0.f;
-        gate[kGateOffBeta + tid] = bg[tid];
-        gate[kGateOffG + tid] = bg[kKMax + tid];
-      }
-      if (tid < kGateFloats - (kGateOffGam + kKMax)) gate[kGateOffGam + kKMax + tid] = 0.f;
-    }
+    for (int hv = hv0; hv < min(r, hv0 + 16); ++hv)
+      gate_block<kTree>(p, tree, sBG + (hv - hv0) * 2 * kKMax, kk, kq,
+                        p.ws.gate + (size_t(b) * p.Hv + kh * r + hv) * kGateFloats, tid);
   }
   // the state kernel's independent work (S0 copy, v-channel conv) starts as this grid finishes;
   // earlier starts only made the two grids contend for the SMs (measured)
