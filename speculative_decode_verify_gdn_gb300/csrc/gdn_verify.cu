@@ -298,9 +298,10 @@ __device__ __forceinline__ void qk_norms(const float* sY, int ys, float* sT, flo
 
 // Gram products from the raw rows: thread (n, j) takes row n of [k; q] against k rows j and j + 8
 // (a warp reads four n rows and sixteen k rows, all four banks apart when ys = DK + 4), paired f32
-// FMAs; scaled by the two inverse norms into KK[t][j] = k^_t . k^_j and KQ[t][j] = k^_j . q^_t.
+// FMAs.  qk_gram_raw returns the two unscaled sums; qk_gram_store scales them by the two inverse
+// norms into KK[t][j] = k^_t . k^_j and KQ[t][j] = k^_j . q^_t.
 template <int DK>
-__device__ __forceinline__ void qk_gram(const float* sY, int ys, const float* sInv, float* sKK, float* sKQ, int tid) {
+__device__ __forceinline__ float2 qk_gram_raw(const float* sY, int ys, int tid) {
   const int n = tid >> 3, j = tid & 7;
   const float* yn = sY + n * ys;
   const float* ya = sY + j * ys;
@@ -316,11 +317,15 @@ __device__ __forceinline__ void qk_gram(const float* sY, int ys, const float* sI
     a1 = __ffma2_rn(make_float2(x.x, x.y), make_float2(v.x, v.y), a1);
     a1 = __ffma2_rn(make_float2(x.z, x.w), make_float2(v.z, v.w), a1);
   }
+  return make_float2(a0.x + a0.y, a1.x + a1.y);
+}
+
+__device__ __forceinline__ void qk_gram_store(float2 raw, const float* sInv, float* sKK, float* sKQ, int tid) {
+  const int n = tid >> 3, j = tid & 7;
   const float sn = sInv[n];
-  const float v0 = (a0.x + a0.y) * sn * sInv[j], v1 = (a1.x + a1.y) * sn * sInv[j + 8];
   float* dst = (n < kKMax) ? sKK + n * kMStride : sKQ + (n - kKMax) * kMStride;
-  dst[j] = v0;
-  dst[j + 8] = v1;
+  dst[j] = raw.x * sn * sInv[j];
+  dst[j + 8] = raw.y * sn * sInv[j + 8];
 }
 
 // One v-head's gate block, thread (t, j) = (tid / 16, tid % 16) of 256: M = D o (k^.k^) strictly
@@ -464,8 +469,10 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
   }
   __syncthreads();
 
-  // a2: L2 norm of each of the 2K vectors, straight into the swizzled table (and k^ token-major
-  // to the workspace, for the state updates); a3 for up to 16 v-heads alongside
+  // the Gram products of the raw rows, then a2: the L2 norm of each of the 2K vectors, straight into
+  // the swizzled table (and k^ token-major to the workspace, for the state updates), and a3 for up
+  // to 16 v-heads, all in one phase (the Gram sums are scaled by the inverse norms after it)
+  const float2 graw = qk_gram_raw<DK>(sY, L::YS, tid);
   qk_norms<DK>(sY, L::YS, sT, sInv, p.ws.kn + head * kKMax * DK, K, p.l2_eps, warp, lane);
   gate_store(0);
   __syncthreads();
@@ -480,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
     }
   }
 
-  qk_gram<DK>(sY, L::YS, sInv, sKK, sKQ, tid);
+  qk_gram_store(graw, sInv, sKK, sKQ, tid);
   __syncthreads();
 
   // per-v-head gate blocks
@@ -574,18 +581,27 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   }
   if constexpr (kGated) cluster_arrive_relaxed();  // this CTA runs: the head's peers may write its smem later
   __syncthreads();  // the barrier is ready before any thread uses it
-  if (warp == 0) {
-    if (lane == 0) mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES);
+  if (tid == 0) {
+    mbar_arrive_expect_tx(bar, L::S0_BYTES + L::WT_BYTES + L::GATE_BYTES + L::KN_BYTES);
+    griddep_wait();  // the prologue grid has finished and its tables are visible
+    const size_t head = size_t(b) * p.Hk + kh;
+    bulk_load(sWT, p.ws.wt + head * DK * kNCol, L::WT_BYTES, bar);
+    bulk_load(sGate, p.ws.gate + (size_t(b) * p.Hv + h) * kGateFloats, L::GATE_BYTES, bar);
+    bulk_load(sKn, p.ws.kn + head * kKMax * DK, L::KN_BYTES, bar);
+  }
+  if (warp == kWarps - 1) {
     // S0: the previous final state, or (rollback applied on read) the accepted intermediate or
     // the pre-window snapshot of the previous window; one row per lane, into rows padded by four
-    // banks so that the four rows a warp reads together in the products below do not conflict
+    // banks so that the four rows a warp reads together in the products below do not conflict.
+    // (A warp of its own, so that the tables' copies above do not wait behind the load of the
+    // accept length; the copies' bytes may land before the expected count is set, the phase
+    // completing only with thread 0's arrival.)
     const int Lp = prev_accept(p, b, blockIdx.x == 0 && lane == 0);
     const float* s0 = p.state_in + tile_off;
     if (Lp == 0)
       s0 = p.state_snap_prev + tile_off;
     else if (Lp > 0 && Lp < K)
       s0 = p.state_inter_prev + (size_t(b) * (K - 1) + (Lp - 1)) * size_t(p.Hv) * DV * DK + (size_t(h) * DV + r0) * DK;
-    __syncwarp();  // (the expected byte count is set before any row can land)
     bulk_load(sS0 + lane * L::SSTRIDE, s0 + size_t(lane) * DK, L::S0_ROW_BYTES, bar);
   }
   // gated: the lane's two z values of the epilogue, (token cg, row m of its warp) and eight tokens
@@ -603,13 +619,6 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_state_stream_kernel(const Ver
   if constexpr (kTree) {  // (off thread 0, and before it waits for the prologue grid)
     if (tid == 32) build_tree(p, b, tree, false);
     __syncthreads();  // the tree table is ready before the conv reads it
-  }
-  if (tid == 0) {
-    griddep_wait();  // the prologue grid has finished and its tables are visible
-    const size_t head = size_t(b) * p.Hk + kh;
-    bulk_load(sWT, p.ws.wt + head * DK * kNCol, L::WT_BYTES, bar);
-    bulk_load(sGate, p.ws.gate + (size_t(b) * p.Hv + h) * kGateFloats, L::GATE_BYTES, bar);
-    bulk_load(sKn, p.ws.kn + head * kKMax * DK, L::KN_BYTES, bar);
   }
 
   // a1 for this CTA's v-channels: lanes 4..7 of warp w convolve rows 4w..4w+3
