@@ -263,6 +263,13 @@ gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t s
   p.q_scale = d.q_scale;
   p.l2_eps = d.l2_eps;
   p.out_f32 = d.out_f32;
+  {
+    // the prologue grid (B * Hk CTAs) fills at most half the SMs: let the state kernel start early
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      p.early_dependents = (long long)d.B * d.Hk * 2 <= sms;
+  }
   cudaError_t e = gdn::launch_verify(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "verify launch: %s", cudaGetErrorString(e));
   return ok();

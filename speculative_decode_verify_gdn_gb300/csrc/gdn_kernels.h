@@ -69,6 +69,7 @@ struct VerifyParams {
   int B, K, Hk, Hv, dk, dv, C;
   float q_scale, l2_eps;
   int out_f32;
+  int early_dependents;  // the prologue lets the state kernel launch at its start (small grids)
 };
 
 struct ConvParams {

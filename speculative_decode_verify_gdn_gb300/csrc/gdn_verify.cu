@@ -412,6 +412,10 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
   const int K = p.K;
   const int r = p.Hv / p.Hk;
   const size_t head = size_t(b) * p.Hk + kh;
+  // a small grid leaves most SMs idle: the state kernel may start on them right away (its S0
+  // copies and v-channel conv then overlap this kernel; it still waits for this grid to complete
+  // before it reads the tables)
+  if (p.early_dependents) griddep_launch_dependents();
 
   // a3 inputs of up to 16 v-heads (thread = (head, token)), loaded first so that their latency
   // overlaps the conv's loads; the gates are evaluated once the conv is done
@@ -504,9 +508,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_qk_prologue_kernel(const Veri
       gate_block<kTree>(p, tree, sBG + (hv - hv0) * 2 * kKMax, kk, kq,
                         p.ws.gate + (size_t(b) * p.Hv + kh * r + hv) * kGateFloats, tid);
   }
-  // the state kernel's independent work (S0 copy, v-channel conv) starts as this grid finishes;
-  // earlier starts only made the two grids contend for the SMs (measured)
-  griddep_launch_dependents();
+  // on a large grid the state kernel's independent work (S0 copy, v-channel conv) starts as this
+  // grid finishes: earlier starts only made the two grids contend for the SMs (measured)
+  if (!p.early_dependents) griddep_launch_dependents();
 }
 
 // ------------------------------------------------------------------------------------------
