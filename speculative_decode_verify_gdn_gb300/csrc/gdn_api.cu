@@ -264,11 +264,14 @@ gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t s
   p.l2_eps = d.l2_eps;
   p.out_f32 = d.out_f32;
   {
-    // the prologue grid (B * Hk CTAs) fills at most half the SMs: let the state kernel start early
+    // the prologue grid (B * Hk CTAs) fills at most an eighth of the SMs: let the state kernel start
+    // early.  Measured at Hk = 16 on one GB300: B = 1 gains (K = 16 rounds 20.5 -> 18.6 us, graph-
+    // replayed decode 11.6 -> 9.7 us); with the switch at half the SMs, B = 2, K = 16 lost
+    // (26.7 -> 30.8 us) and B = 4 did not change
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-      p.early_dependents = (long long)d.B * d.Hk * 2 <= sms;
+      p.early_dependents = (long long)d.B * d.Hk * 8 <= sms;
   }
   cudaError_t e = gdn::launch_verify(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "verify launch: %s", cudaGetErrorString(e));
