@@ -26,6 +26,11 @@
  *  - Ownership: the caller owns every buffer, scratch included.  The library
  *    allocates and frees nothing; its only state is a thread-local error
  *    message and one 32-bit device status word per GPU (see gdn_device_status).
+ *  - Device reset: the library caches, per device, the device addresses of
+ *    its status word and of gdn_verify_step_static_scratch's array, looked up
+ *    on first use.  Do not call it across a cudaDeviceReset (or anything else
+ *    that destroys and recreates the device's primary context) in one process:
+ *    the cached addresses would point into the old context.
  *  - Asynchrony: calls validate on the host, enqueue kernels on `stream` and
  *    return; launch failures come back as GDN_ERR_CUDA.
  *  - Validation happens before any launch: a non-OK status means nothing was
