@@ -799,9 +799,10 @@ def run_only(args):
         ms = ctx.timed(lambda i: lay.resume(win, i % win.n, (i - 1) % win.n, ctx.stream), args.steps,
                        warmup=args.warmup, first=1)
     else:
-        def tree_step(i, parent=torch.from_numpy(
-                __import__("speculative_decode_verify_gdn_gb300.synth", fromlist=["make_tree"]).make_tree(
-                    Gen(w.seed + 77), w.dims.B, w.dims.K, 0.5)).to(ctx.dev)):
+        from speculative_decode_verify_gdn_gb300.synth import make_tree
+        parent = torch.from_numpy(make_tree(Gen(w.seed + 77), w.dims.B, w.dims.K, 0.5)).to(ctx.dev)
+
+        def tree_step(i):
             j = i % win.n
             gdn.gdn_verify_tree(lay.dims, parent, win.x[j], win.a[j], win.b[j], lay.A_log, lay.dt_bias, lay.conv_w,
                                 lay.CS, lay.CS, lay.CI, lay.S, lay.S, lay.SI, lay.out, lay.ws, ctx.stream)
