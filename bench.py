@@ -45,7 +45,7 @@ UNIT = "tokens/s"
 WORKLOAD = "serve16"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_SIDECAR = os.path.join(ROOT, "profiles", "verify_traffic.json")
-LAUNCHES_PER_STEP = 2   # q/k prologue, state stream (the rollback is applied on read)
+LAUNCHES_PER_STEP = 2   # verify, q|k history (the rollback is applied on read)
 N_WINDOWS = 8           # distinct windows resident in HBM, cycled through the steps
 SIDE_MIN_STEPS = 200    # floor of timed work of every side measurement ...
 SIDE_MIN_SECONDS = 0.25  # ... in steps and in seconds, whichever is more
@@ -654,8 +654,8 @@ def run_gdn(args):
         "config": headline_config(world),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": profile_traffic(digest),
-                     "kernel": "gdn_verify_resume (gdn_qk_prologue_kernel + gdn_state_stream_kernel, overlapped "
-                               "through programmatic dependent launch)",
+                     "kernel": "gdn_verify_resume (gdn_verify_kernel + gdn_qk_history_kernel, the second "
+                               "started by programmatic dependent launch inside the first)",
                      "algorithmic_bytes_per_launch": vbytes, "launch_ms": call_ms,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s", "kernel_digest": digest},

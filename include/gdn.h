@@ -113,15 +113,16 @@ gdn_status gdn_conv_step(const gdn_dims* dims, const uint16_t* x, const float* c
  *   state_inter     [B, K-1, Hv, dv, dk] f32: state after tokens 0..K-2;
  *                                     NULL allowed only when K == 1
  *   out             [B, K, Hv, dv]    bf16 or f32 (out_f32): o_t = q_scale * S_t q_t
- *   workspace       device scratch of at least gdn_verify_workspace_size() bytes,
- *                   16-byte aligned; holds the normalised q/k, Gram products and
- *                   gates that pass from the q/k prologue kernel to the state
- *                   kernel.  Contents need no initialisation and are dead after the
- *                   call; calls that overlap on the GPU must not share it.
- * Intermediates, out and workspace must not overlap any other buffer.
- * Runs as two kernels on `stream`: a per-(sequence, q/k head) prologue and a
- * per-(sequence, v-head, 32-row tile) state kernel started with programmatic
- * dependent launch.
+ *   workspace       unused: gdn_verify_workspace_size() reports 0 bytes and the
+ *                   pointer may be NULL (the argument keeps the ABI of earlier
+ *                   builds, whose kernels passed tables through it).
+ * Intermediates and out must not overlap any other buffer.
+ * Runs as two kernels on `stream`: a per-(sequence, v-head, 32-row tile)
+ * verify kernel (conv, norms, gates and the state recurrence, which stores
+ * every state straight from registers) and a per-(sequence, q/k channel
+ * block) kernel that writes the q|k channels' history snapshots and new
+ * history once every verify CTA has read the old ones (programmatic
+ * dependent launch).  The call is complete when the second kernel is.
  */
 gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16_t* a, const uint16_t* b,
                            const float* A_log, const float* dt_bias, const float* conv_w,
@@ -147,8 +148,10 @@ gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16
  * In place is allowed and is the intended use: state_out may be state_in or
  * state_snapshot_prev, state_inter may be state_inter_prev, conv_state_out may
  * be conv_state_in or conv_state_snapshot_prev, conv_inter may be
- * conv_inter_prev (each state tile and history channel is read, then
- * rewritten, by one owner).  Any other overlap with an output is rejected.
+ * conv_inter_prev (each state tile and v-channel history is read, then
+ * rewritten, by one owner; the q|k channels' history, which every CTA of a q/k
+ * head reads, is rewritten by the second kernel only after all those reads).
+ * Any other overlap with an output is rejected.
  * Shapes, workspace and the remaining arguments as gdn_verify_step.
  */
 gdn_status gdn_verify_resume(const gdn_dims* dims, const int32_t* accept_len_prev, const uint16_t* x,
@@ -205,8 +208,8 @@ gdn_status gdn_verify_gated(const gdn_dims* dims, const uint16_t* x, const uint1
                             uint64_t workspace_bytes, gdn_stream_t stream);
 
 /*
- * Bytes of workspace gdn_verify_step needs for `dims`:
- * 4 * (B*Hk*(32*dk + 16*dk) + B*Hv*596).  Validates dims like gdn_verify_step.
+ * Bytes of workspace gdn_verify_step needs for `dims`: 0 (its kernels share
+ * nothing through global scratch).  Validates dims like gdn_verify_step.
  */
 gdn_status gdn_verify_workspace_size(const gdn_dims* dims, uint64_t* bytes);
 
@@ -218,16 +221,14 @@ gdn_status gdn_verify_workspace_size(const gdn_dims* dims, uint64_t* bytes);
  * callers may not call cudaMalloc where they run the verify step (a runtime
  * whose memory pool forbids allocation on its hot path, a path that must not
  * synchronise the device, an embedder that only passes in tensors it owns);
- * this entry point takes its scratch from a fixed 16 MiB array in the
- * library's device memory instead, enough for B = 32 at Hk = 16, Hv = 32,
- * dk = 128.  Every GPU that loads the library holds that array until the
- * process exits.  Larger dims return GDN_ERR_UNSUPPORTED with a message.
+ * this entry point passes a fixed array in the library's device memory as the
+ * workspace instead.  The verify kernels need no scratch (see
+ * gdn_verify_workspace_size), so the array is 256 bytes; dims that would need
+ * more return GDN_ERR_UNSUPPORTED with a message.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress) with that device current and caches it: make the
  *    first call on a device before any stream capture starts.
- *  - The scratch needs no zeroing; nothing is allocated or freed.
- *  - All calls on a device share the array: calls whose kernels may overlap
- *    on the GPU (unordered streams) race on it and must be serialised.
+ *  - Nothing is allocated or freed.
  */
 gdn_status gdn_verify_step_static_scratch(const gdn_dims* dims, const uint16_t* x, const uint16_t* a,
                                           const uint16_t* b, const float* A_log, const float* dt_bias,

@@ -123,8 +123,6 @@ struct VerifyArgs {
   float* state_out;
   float* state_inter;
   void* out;
-  void* workspace;
-  uint64_t workspace_bytes;
 };
 
 struct Buf {
@@ -151,7 +149,6 @@ gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t s
   GDN_CHECK_PTR(v.state_out, "state_out");
   GDN_CHECK_OPT_PTR(v.state_inter, "state_inter");
   GDN_CHECK_PTR(v.out, "out");
-  GDN_CHECK_PTR(v.workspace, "workspace");
   if (d.K > 1 && !v.state_inter) return fail(GDN_ERR_INVALID_ARG, "state_inter is NULL with K=%d > 1", d.K);
   if (v.resume) {
     if (!v.accept_prev) return fail(GDN_ERR_INVALID_ARG, "accept_len_prev is NULL");
@@ -172,10 +169,6 @@ gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t s
     if (!std::isfinite(v.norm_eps) || v.norm_eps < 0.f)
       return fail(GDN_ERR_INVALID_ARG, "norm_eps must be finite, >= 0");
   }
-  const size_t ws_need = gdn::workspace_bytes(d.B, d.Hk, d.Hv, d.dk);
-  if (v.workspace_bytes < ws_need)
-    return fail(GDN_ERR_INVALID_ARG, "workspace has %llu bytes, needs %zu", (unsigned long long)v.workspace_bytes,
-                ws_need);
 
   const size_t C = 2ull * d.Hk * d.dk + size_t(d.Hv) * d.dv;
   const size_t B = size_t(d.B), K = size_t(d.K);
@@ -203,7 +196,6 @@ gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t s
       {"state_out", range_of(v.state_out, B * S * 4), true},
       {"state_inter", range_of(k1 ? nullptr : v.state_inter, B * (K - 1) * S * 4), true},
       {"out", range_of(v.out, B * K * d.Hv * d.dv * (d.out_f32 ? 4 : 2)), true},
-      {"workspace", range_of(v.workspace, ws_need), true},
   };
   // (output, input) pairs that may be the very same buffer: every state tile and every history
   // channel is read, then rewritten, by one owner, so working in place is race-free
@@ -240,7 +232,6 @@ gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t s
   p.state_out = v.state_out;
   p.state_inter = k1 ? nullptr : v.state_inter;
   p.out = v.out;
-  p.ws = gdn::workspace_carve(v.workspace, d.B, d.Hk, d.Hv, d.dk);
   p.parent = v.parent;
   p.z = v.z;
   p.norm_w = v.z ? v.norm_w : nullptr;
@@ -263,16 +254,6 @@ gdn_status verify_impl(const gdn_dims* dims, const VerifyArgs& v, gdn_stream_t s
   p.q_scale = d.q_scale;
   p.l2_eps = d.l2_eps;
   p.out_f32 = d.out_f32;
-  {
-    // the prologue grid (B * Hk CTAs) fills at most an eighth of the SMs: let the state kernel start
-    // early.  Measured at Hk = 16 on one GB300: B = 1 gains (K = 16 rounds 20.5 -> 18.6 us, graph-
-    // replayed decode 11.6 -> 9.7 us); with the switch at half the SMs, B = 2, K = 16 lost
-    // (26.7 -> 30.8 us) and B = 4 did not change
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-      p.early_dependents = (long long)d.B * d.Hk * 8 <= sms;
-  }
   cudaError_t e = gdn::launch_verify(p, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(GDN_ERR_CUDA, "verify launch: %s", cudaGetErrorString(e));
   return ok();
@@ -335,7 +316,7 @@ gdn_status gdn_verify_workspace_size(const gdn_dims* dims, uint64_t* bytes) {
   gdn_status s = check_dims(dims, true);
   if (s != GDN_OK) return s;
   if (!bytes) return fail(GDN_ERR_INVALID_ARG, "bytes is NULL");
-  *bytes = gdn::workspace_bytes(dims->B, dims->Hk, dims->Hv, dims->dk);
+  *bytes = 0;  // the verify kernels keep everything they share in shared memory
   return ok();
 }
 
@@ -358,8 +339,8 @@ gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16
   v.state_out = state_out;
   v.state_inter = state_inter;
   v.out = out;
-  v.workspace = workspace;
-  v.workspace_bytes = workspace_bytes;
+  (void)workspace;  // (needs 0 bytes: see gdn_verify_workspace_size)
+  (void)workspace_bytes;
   return verify_impl(dims, v, stream);
 }
 
@@ -384,8 +365,8 @@ gdn_status gdn_verify_tree(const gdn_dims* dims, const int32_t* parent_dev, cons
   v.state_out = state_out;
   v.state_inter = state_inter;
   v.out = out;
-  v.workspace = workspace;
-  v.workspace_bytes = workspace_bytes;
+  (void)workspace;  // (needs 0 bytes: see gdn_verify_workspace_size)
+  (void)workspace_bytes;
   return verify_impl(dims, v, stream);
 }
 
@@ -413,8 +394,8 @@ gdn_status gdn_verify_gated(const gdn_dims* dims, const uint16_t* x, const uint1
   v.state_out = state_out;
   v.state_inter = state_inter;
   v.out = out;
-  v.workspace = workspace;
-  v.workspace_bytes = workspace_bytes;
+  (void)workspace;  // (needs 0 bytes: see gdn_verify_workspace_size)
+  (void)workspace_bytes;
   return verify_impl(dims, v, stream);
 }
 
@@ -445,8 +426,8 @@ gdn_status gdn_verify_resume(const gdn_dims* dims, const int32_t* accept_len_pre
   v.state_out = state_out;
   v.state_inter = state_inter;
   v.out = out;
-  v.workspace = workspace;
-  v.workspace_bytes = workspace_bytes;
+  (void)workspace;  // (needs 0 bytes: see gdn_verify_workspace_size)
+  (void)workspace_bytes;
   return verify_impl(dims, v, stream);
 }
 

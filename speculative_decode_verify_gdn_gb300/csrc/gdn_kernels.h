@@ -11,28 +11,7 @@ namespace gdn {
 
 constexpr int kKMax = 16;  // longest verify window a launch handles
 constexpr int kConvW = 4;  // conv taps
-constexpr int kNCol = 2 * kKMax;  // columns of the normalised q/k table: k^ in [0,16), q^ in [16,32)
-constexpr int kMStride = kKMax + 1;
-// Per-(sequence, v-head) gate block: M[16][17] = D (k^.k^) strictly lower, N[16][17] =
-// q_scale D (k^.q^) lower, beta[16], g[16], Gamma[16], padding (D: decay products).
-constexpr int kGateFloats = 2 * kKMax * kMStride + 3 * kKMax + 4;  // 596 floats = 2384 bytes (16-byte multiple)
-constexpr int kGateOffN = kKMax * kMStride;
-constexpr int kGateOffBeta = 2 * kKMax * kMStride;
-constexpr int kGateOffG = kGateOffBeta + kKMax;
-constexpr int kGateOffGam = kGateOffG + kKMax;
-
-// Workspace written by the q/k prologue kernel and read by the state kernel:
-//   wt    [B][Hk][dk][32]     normalised k^ (columns 0..15) and q^ (16..31)
-//   kn    [B][Hk][16][dk]     normalised k^, token-major
-//   gate  [B][Hv][kGateFloats]
-struct Workspace {
-  float* wt;
-  float* kn;
-  float* gate;
-};
-
-size_t workspace_bytes(int B, int Hk, int Hv, int dk);
-Workspace workspace_carve(void* base, int B, int Hk, int Hv, int dk);
+constexpr int kNCol = 2 * kKMax;  // rows of a window's q/k table: k^ in [0,16), q^ in [16,32)
 
 struct VerifyParams {
   const uint16_t* x;
@@ -48,7 +27,6 @@ struct VerifyParams {
   float* state_out;
   float* state_inter;  // null only when K == 1
   void* out;
-  Workspace ws;
   // Rollback of the previous window applied on read (all null for a plain verify step): per
   // sequence, L = accept_prev[b] selects where S0 and the conv history come from -
   // L == K: state_in / conv_state_in (the previous window's final state and history);
@@ -69,7 +47,6 @@ struct VerifyParams {
   int B, K, Hk, Hv, dk, dv, C;
   float q_scale, l2_eps;
   int out_f32;
-  int early_dependents;  // the prologue lets the state kernel launch at its start (small grids)
 };
 
 struct ConvParams {

@@ -3,21 +3,18 @@
 // Some callers are not allowed to call cudaMalloc (or any allocator) at the point where they
 // run the verify step: code inside a memory-pool-managed runtime that forbids allocations on
 // its hot path, code paths that must not synchronise the device (cudaMalloc/cudaFree may), or
-// embedders that only hand this library the tensors they already own.  They still need the
-// scratch that gdn_verify_step takes as its `workspace` argument.  This file supplies that
-// scratch from a fixed array in the library's own device memory instead.
+// embedders that only hand this library the tensors they already own.  This entry point passes
+// a fixed array in the library's own device memory as gdn_verify_step's `workspace` argument,
+// so such callers never size or allocate one.  The verify kernels need no scratch at all
+// (gdn_verify_workspace_size reports 0 bytes), so the array is small; should a shape ever need
+// more than it holds, the call returns GDN_ERR_UNSUPPORTED instead of running.
 //
 // The array is a file-scope __device__ variable, so every GPU on which the library's module is
-// loaded holds kStaticScratchBytes of device memory for it until the process exits.  Host code
-// cannot use the array's name as a device address (on the host it names a shadow variable), so
-// the device address is looked up with cudaGetSymbolAddress once per device, with that device
-// current, on the first call made on that device, and cached.  Make that first call before any
-// stream capture begins, so the lookup does not happen inside a capture.
-//
-// The scratch needs no initialisation: within one call the q/k prologue kernel writes every
-// byte the state kernel reads before the state kernel reads it.  All calls on a device share
-// the one array, so two calls whose kernels may overlap on that GPU (different streams without
-// ordering between them) race on it; serialise them.
+// loaded holds it until the process exits.  Host code cannot use the array's name as a device
+// address (on the host it names a shadow variable), so the device address is looked up with
+// cudaGetSymbolAddress once per device, with that device current, on the first call made on
+// that device, and cached.  Make that first call before any stream capture begins, so the
+// lookup does not happen inside a capture.
 #include <cstdio>
 #include <mutex>
 
@@ -26,9 +23,8 @@
 
 namespace {
 
-// Largest scratch the fixed array provides: enough for the serving shape
-// (B=32, Hk=16, Hv=32, dk=128: 15,024,128 bytes).
-constexpr size_t kStaticScratchBytes = size_t(16) << 20;  // 16 MiB
+// Largest scratch the fixed array provides.
+constexpr size_t kStaticScratchBytes = 256;
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 

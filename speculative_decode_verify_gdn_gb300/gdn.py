@@ -269,9 +269,8 @@ def gdn_verify_resume(dims: GdnDims, accept_len_prev, x, a, b, A_log, dt_bias, c
 def gdn_verify_step_static_scratch(dims: GdnDims, x, a, b, A_log, dt_bias, conv_w, conv_state_in, conv_state_out,
                                    conv_inter, state_in, state_out, state_inter, out, stream=None) -> None:
     """gdn_verify_step without a workspace argument, for callers that must not allocate device memory:
-    the scratch is a fixed 16 MiB array inside the library (B <= 32 at the 16/32-head, 128-dim shape).
-    The first call on a device looks the array up; make it before any stream capture.  Calls that can
-    overlap on one GPU share the array and must be serialised."""
+    a fixed array inside the library stands in for the workspace (the verify kernels need none).  The
+    first call on a device looks the array up; make it before any stream capture."""
     d = dims
     C, BK = d.C, d.B * d.K
     S = d.Hv * d.dv * d.dk

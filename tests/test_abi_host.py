@@ -45,7 +45,7 @@ def _ptrs(n, step=MB):
     return [ctypes.c_void_p(P + i * step) for i in range(n)]
 
 
-NV = 14              # pointer arguments of gdn_verify_step (the 14th is the workspace)
+NV = 14              # pointer arguments of gdn_verify_step (the 14th is the workspace, which is unused)
 
 
 def _verify(lib, dims, ptrs, ws_bytes=1 << 40):
@@ -81,7 +81,7 @@ def test_empty_batch_is_a_noop(lib):
 
 def test_null_and_misaligned_pointers(lib):
     dims = gdn.make_dims(**BASE)
-    for i in range(NV):
+    for i in range(NV - 1):   # (every call here must fail validation: the pointers are not real)
         if i in (8,):          # conv_inter is optional
             continue
         ptrs = _ptrs(NV)
@@ -115,18 +115,11 @@ def test_aliasing_rules(lib):
     ptrs = _ptrs(NV)
     ptrs[11] = None
     assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_INVALID_ARG
-    # workspace overlapping out, and a workspace that is too small
-    ptrs = _ptrs(NV)
-    ptrs[13] = ptrs[12]
-    assert _verify(lib, dims, ptrs) == gdn.GDN_ERR_ALIAS
-    ptrs = _ptrs(NV)
-    assert _verify(lib, dims, ptrs, ws_bytes=64) == gdn.GDN_ERR_INVALID_ARG
-    assert "workspace" in gdn.last_error()
 
 
 def test_workspace_size_formula(lib):
     dims = gdn.make_dims(B=32, K=16, Hk=16, Hv=32, dk=128, dv=128)
-    assert gdn.gdn_verify_workspace_size(dims) == 4 * (32 * 16 * (32 * 128 + 16 * 128) + 32 * 32 * 596)
+    assert gdn.gdn_verify_workspace_size(dims) == 0   # the verify kernels share nothing through global scratch
     with pytest.raises(gdn.GdnError):
         gdn.gdn_verify_workspace_size(gdn.make_dims(B=1, K=0, Hk=1, Hv=1, dk=64, dv=64))
 

@@ -79,7 +79,7 @@ def test_shapes_against_oracle(shape, out_f32):
 
 
 def test_many_vheads_per_qk_head():
-    """Hv/Hk = 8: one q/k head feeds eight v-heads (the prologue writes eight gate blocks)."""
+    """Hv/Hk = 8: one q/k head feeds eight v-heads (32 verify CTAs convolve and normalise its q|k)."""
     d = Dims(B=2, K=6, Hk=1, Hv=8, dk=128, dv=128)
     g = Gen(77)
     lay = make_layer(g, d, Dists())
