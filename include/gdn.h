@@ -174,7 +174,8 @@ gdn_status gdn_verify_resume(const gdn_dims* dims, const int32_t* accept_len_pre
  * (state_inter[b][t] for t < K-1, state_out / conv_state_out for node K-1,
  * conv_inter[b][t]), so gdn_rollback with accept_len = n + 1 rolls a sequence
  * back to accepted node n (0 for none).  A chain (parent[t] = t-1) gives
- * gdn_verify_step's results.  A parent outside -1..t-1 is read as -1 and sets
+ * gdn_verify_step's histories bit for bit and its states and outputs up to
+ * f32 rounding order.  A parent outside -1..t-1 is read as -1 and sets
  * GDN_DEVERR_TREE_PARENT.  Other arguments, aliasing and workspace as
  * gdn_verify_step.
  */

@@ -260,6 +260,86 @@ __device__ __forceinline__ void raw_gate(float a, float b, float A_log, float dt
 }
 
 
+// The V = dk / 32 state columns a lane holds per row (a4): 16-byte pieces at dk = 128, 8-byte
+// at dk = 64.
+template <int V>
+__device__ __forceinline__ void load_vec(const float* src, float (&v)[V]) {
+  if constexpr (V == 4) {
+    const float4 x = *reinterpret_cast<const float4*>(src);
+    v[0] = x.x;
+    v[1] = x.y;
+    v[2] = x.z;
+    v[3] = x.w;
+  } else {
+    static_assert(V == 2, "dk = 128 or 64");
+    const float2 x = *reinterpret_cast<const float2*>(src);
+    v[0] = x.x;
+    v[1] = x.y;
+  }
+}
+
+template <int V>
+__device__ __forceinline__ float dot_vec(const float (&s)[V], const float (&k)[V]) {
+  if constexpr (V == 4) {
+    float2 acc = __fmul2_rn(make_float2(s[0], s[1]), make_float2(k[0], k[1]));
+    acc = __ffma2_rn(make_float2(s[2], s[3]), make_float2(k[2], k[3]), acc);
+    return acc.x + acc.y;
+  } else {
+    return fmaf(s[1], k[1], s[0] * k[0]);
+  }
+}
+
+// s = g s + u k, two lanes of f32 per instruction
+template <int V>
+__device__ __forceinline__ void update_vec(float (&s)[V], float g, float u, const float (&k)[V]) {
+  const float2 gg = make_float2(g, g), uu = make_float2(u, u);
+#pragma unroll
+  for (int e = 0; e < V; e += 2) {
+    const float2 r = __ffma2_rn(uu, make_float2(k[e], k[e + 1]), __fmul2_rn(gg, make_float2(s[e], s[e + 1])));
+    s[e] = r.x;
+    s[e + 1] = r.y;
+  }
+}
+
+// streaming (evict-first) unless `keep`
+template <int V>
+__device__ __forceinline__ void store_vec(float* dst, const float (&v)[V], bool keep) {
+  if constexpr (V == 4) {
+    const float4 x = make_float4(v[0], v[1], v[2], v[3]);
+    if (keep)
+      *reinterpret_cast<float4*>(dst) = x;
+    else
+      __stcs(reinterpret_cast<float4*>(dst), x);
+  } else {
+    const float2 x = make_float2(v[0], v[1]);
+    if (keep)
+      *reinterpret_cast<float2*>(dst) = x;
+    else
+      __stcs(reinterpret_cast<float2*>(dst), x);
+  }
+}
+
+// For every lane l, the sum over the warp's 32 lanes of p[l / 8]: two halving rounds (partners
+// 16, then 8 lanes apart, each lane keeping half of the rows it still holds and sending the other
+// half) and a butterfly over the last three lane bits, 6 shuffles in all.  The eight lanes of a
+// row end with the same value (each pairwise sum adds the same two numbers).
+__device__ __forceinline__ float reduce4(const float (&p)[4], int lane) {
+  const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+  float k0 = h16 ? p[2] : p[0];
+  float k1 = h16 ? p[3] : p[1];
+  const float x0 = h16 ? p[0] : p[2];
+  const float x1 = h16 ? p[1] : p[3];
+  k0 += __shfl_xor_sync(0xffffffffu, x0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, x1, 16);
+  float k = h8 ? k1 : k0;
+  const float x = h8 ? k0 : k1;
+  k += __shfl_xor_sync(0xffffffffu, x, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  return k;
+}
+
 // ------------------------------------------------------------------------------------------
 // Kernel 2: the q|k channels' history snapshots and new history (thread = channel pair 2i, 2i+1
 // of the 2 Hk dk q|k channels, q first).  Snapshot t of a chain window is the history after token
@@ -488,112 +568,162 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyPar
     if constexpr (!kGated) return;
   }
 
-  // a4: lane (m, cg) holds row warp*4 + m of the tile at columns 32 f + 4 cg .. + 3 (f < dk/32);
-  // o_a, o_b keep o of tokens cg and cg + 8 of that row for the epilogue
-  constexpr int F = DK / 32;
+  // a4.  Lane (m, cg) = (l / 8, l % 8) keeps o of row 4 warp + m for tokens cg and cg + 8 for the
+  // epilogue.  A chain window holds row m at columns 32 f + 4 cg .. + 3 (f < dk / 32), the row's
+  // dot products then needing only its eight lanes (three shuffles on the path from one token to
+  // the next); a token tree holds all four rows of the warp at columns V l .. V l + V - 1 (V = dk /
+  // 32), so that the k^ reads of its branch rebuilds are 32 distinct pieces instead of the same
+  // 128 bytes read by four row groups, at the price of a reduction over the whole warp per dot
+  // product (reduce4).  Measured at the serving shape: the tree layout took seeded 16-node trees
+  // from 230.1 to 213.3 us per step, and made the chain's latency-bound shapes slower (B = 32,
+  // K = 8 rounds 109.4 -> 114.7 us, the gated variant 191.8 -> 196.4 us).
   const int m = lane >> 3;
   const int cg = lane & 7;
   const int row = warp * kRowsPerWarp + m;
-  const int col = 4 * cg;
   float o_a = 0.f, o_b = 0.f;
+  const size_t inter_stride = size_t(p.Hv) * DV * DK;
   if (ok) {
     (void)mbar_try_wait(bar, 0);  // every lane observes the completed phase
-    const float* s0r = sS0 + row * L::SSTRIDE + col;
-    float4 s[F];
+    if constexpr (kTree) {
+      constexpr int V = DK / 32;
+      const int row0 = warp * kRowsPerWarp;
+      const int col = V * lane;
+      float s[kRowsPerWarp][V];
 #pragma unroll
-    for (int f = 0; f < F; ++f) s[f] = *reinterpret_cast<const float4*>(s0r + 32 * f);
-    const size_t inter_stride = size_t(p.Hv) * DV * DK;
-    const size_t my_off = size_t(row) * DK + col;
-    float* fin = p.state_out + tile_off + my_off;
-    float* inter = p.state_inter
-                       ? p.state_inter + size_t(b) * (K - 1) * inter_stride + (size_t(h) * DV + r0) * DK + my_off
-                       : nullptr;
-    for (int t = 0; t < K; ++t) {
-      if constexpr (kTree) {
+      for (int r = 0; r < kRowsPerWarp; ++r) load_vec<V>(sS0 + (row0 + r) * L::SSTRIDE + col, s[r]);
+      const size_t my_off = size_t(row0) * DK + col;
+      float* fin = p.state_out + tile_off + my_off;
+      float* inter = p.state_inter
+                         ? p.state_inter + size_t(b) * (K - 1) * inter_stride + (size_t(h) * DV + r0) * DK + my_off
+                         : nullptr;
+      for (int t = 0; t < K; ++t) {
         // a node that does not continue the previous one starts from its parent's state, rebuilt
         // in its closed form S_par = Gamma_par S0 + sum_{j in path(par)} D[par][j] u_j k^_j^T
         // (D: the product of g over the path nodes after j), walking the path upwards
         const int par = tree->parent[t];
         if (t > 0 && par != t - 1) {
 #pragma unroll
-          for (int f = 0; f < F; ++f) s[f] = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+            for (int e = 0; e < V; ++e) s[r][e] = 0.f;
           float d = 1.f;
           for (int j = par; j >= 0; j = tree->parent[j]) {
-            const float du = d * sU[j * kRows + row];
-            const float* kj = sY + j * L::SSTRIDE + col;
+            const float4 uj = *reinterpret_cast<const float4*>(sU + j * kRows + row0);
+            const float du[kRowsPerWarp] = {d * uj.x, d * uj.y, d * uj.z, d * uj.w};
+            float kj[V];
+            load_vec<V>(sY + j * L::SSTRIDE + col, kj);
 #pragma unroll
-            for (int f = 0; f < F; ++f) {
-              const float4 kv = *reinterpret_cast<const float4*>(kj + 32 * f);
-              s[f].x = fmaf(du, kv.x, s[f].x);
-              s[f].y = fmaf(du, kv.y, s[f].y);
-              s[f].z = fmaf(du, kv.z, s[f].z);
-              s[f].w = fmaf(du, kv.w, s[f].w);
-            }
+            for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+              for (int e = 0; e < V; ++e) s[r][e] = fmaf(du[r], kj[e], s[r][e]);
             d *= sBG[kKMax + j];
           }
 #pragma unroll
-          for (int f = 0; f < F; ++f) {
-            const float4 sv = *reinterpret_cast<const float4*>(s0r + 32 * f);
-            s[f].x = fmaf(d, sv.x, s[f].x);
-            s[f].y = fmaf(d, sv.y, s[f].y);
-            s[f].z = fmaf(d, sv.z, s[f].z);
-            s[f].w = fmaf(d, sv.w, s[f].w);
+          for (int r = 0; r < kRowsPerWarp; ++r) {
+            float sv[V];
+            load_vec<V>(sS0 + (row0 + r) * L::SSTRIDE + col, sv);
+#pragma unroll
+            for (int e = 0; e < V; ++e) s[r][e] = fmaf(d, sv[e], s[r][e]);
           }
         }
-      }
-      // S_{t-1} k^_t over the row: the lane's columns, then the row's eight lanes (every lane of
-      // the row ends with the same sum: the butterfly adds the same pairs in each)
-      const float* kr = sY + t * L::SSTRIDE + col;
-      float4 kv[F];
+        // S_{t-1} k^_t for the four rows (every lane ends with the same four sums)
+        float kv[V];
+        load_vec<V>(sY + t * L::SSTRIDE + col, kv);
+        float pk[kRowsPerWarp];
 #pragma unroll
-      for (int f = 0; f < F; ++f) kv[f] = *reinterpret_cast<const float4*>(kr + 32 * f);
-      float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+        for (int r = 0; r < kRowsPerWarp; ++r) pk[r] = dot_vec<V>(s[r], kv);
+        const float a_m = reduce4(pk, lane);
+        const float g = sBG[kKMax + t];
+        const float beta = sBG[t];
+        const float4 v4 = *reinterpret_cast<const float4*>(sV + t * kRows + row0);
+        const float vr[kRowsPerWarp] = {v4.x, v4.y, v4.z, v4.w};
+        float u[kRowsPerWarp];
 #pragma unroll
-      for (int f = 0; f < F; ++f) {
-        a0 = __ffma2_rn(make_float2(s[f].x, s[f].y), make_float2(kv[f].x, kv[f].y), a0);
-        a1 = __ffma2_rn(make_float2(s[f].z, s[f].w), make_float2(kv[f].z, kv[f].w), a1);
-      }
-      float a = (a0.x + a0.y) + (a1.x + a1.y);
-      a += __shfl_xor_sync(0xffffffffu, a, 1);
-      a += __shfl_xor_sync(0xffffffffu, a, 2);
-      a += __shfl_xor_sync(0xffffffffu, a, 4);
-      const float g = sBG[kKMax + t];
-      const float u = sBG[t] * fmaf(-g, a, sV[t * kRows + row]);
-      if constexpr (kTree) {
-        if (cg == 0) sU[t * kRows + row] = u;
+        for (int r = 0; r < kRowsPerWarp; ++r)
+          u[r] = beta * fmaf(-g, __shfl_sync(0xffffffffu, a_m, 8 * r), vr[r]);
+        if (lane == 0) *reinterpret_cast<float4*>(sU + t * kRows + row0) = make_float4(u[0], u[1], u[2], u[3]);
         __syncwarp();
-      }
-      // S_t = g S_{t-1} + u k^_t, stored straight from registers (the intermediates streaming,
-      // evict-first; the final state with the normal policy)
-      float* dst = (t == K - 1) ? fin : inter + size_t(t) * inter_stride;
-      const float2 gg = make_float2(g, g), uu = make_float2(u, u);
+        // S_t = g S_{t-1} + u k^_t, stored straight from registers (the intermediates streaming,
+        // evict-first; the final state with the normal policy)
+        float* dst = (t == K - 1) ? fin : inter + size_t(t) * inter_stride;
 #pragma unroll
-      for (int f = 0; f < F; ++f) {
-        const float2 lo = __ffma2_rn(uu, make_float2(kv[f].x, kv[f].y), __fmul2_rn(gg, make_float2(s[f].x, s[f].y)));
-        const float2 hi = __ffma2_rn(uu, make_float2(kv[f].z, kv[f].w), __fmul2_rn(gg, make_float2(s[f].z, s[f].w)));
-        s[f] = make_float4(lo.x, lo.y, hi.x, hi.y);
-        float4* d4 = reinterpret_cast<float4*>(dst + 32 * f);
-        if (t == K - 1)
-          *d4 = s[f];
-        else
-          __stcs(d4, s[f]);
-      }
-      // o_t = q_scale S_t q^_t
-      const float* qr = sY + (kKMax + t) * L::SSTRIDE + col;
-      float2 b0 = make_float2(0.f, 0.f), b1 = make_float2(0.f, 0.f);
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+          update_vec<V>(s[r], g, u[r], kv);
+          store_vec<V>(dst + r * DK, s[r], t == K - 1);
+        }
+        // o_t = q_scale S_t q^_t
+        float qv[V];
+        load_vec<V>(sY + (kKMax + t) * L::SSTRIDE + col, qv);
+        float pq[kRowsPerWarp];
 #pragma unroll
-      for (int f = 0; f < F; ++f) {
-        const float4 qv = *reinterpret_cast<const float4*>(qr + 32 * f);
-        b0 = __ffma2_rn(make_float2(s[f].x, s[f].y), make_float2(qv.x, qv.y), b0);
-        b1 = __ffma2_rn(make_float2(s[f].z, s[f].w), make_float2(qv.z, qv.w), b1);
+        for (int r = 0; r < kRowsPerWarp; ++r) pq[r] = dot_vec<V>(s[r], qv);
+        const float o = reduce4(pq, lane) * p.q_scale;
+        if (t == cg) o_a = o;
+        if (t == cg + 8) o_b = o;
       }
-      float o = (b0.x + b0.y) + (b1.x + b1.y);
-      o += __shfl_xor_sync(0xffffffffu, o, 1);
-      o += __shfl_xor_sync(0xffffffffu, o, 2);
-      o += __shfl_xor_sync(0xffffffffu, o, 4);
-      o *= p.q_scale;
-      if (t == cg) o_a = o;
-      if (t == cg + 8) o_b = o;
+    } else {
+      constexpr int F = DK / 32;
+      const int col = 4 * cg;
+      const float* s0r = sS0 + row * L::SSTRIDE + col;
+      float4 s[F];
+#pragma unroll
+      for (int f = 0; f < F; ++f) s[f] = *reinterpret_cast<const float4*>(s0r + 32 * f);
+      const size_t my_off = size_t(row) * DK + col;
+      float* fin = p.state_out + tile_off + my_off;
+      float* inter = p.state_inter
+                         ? p.state_inter + size_t(b) * (K - 1) * inter_stride + (size_t(h) * DV + r0) * DK + my_off
+                         : nullptr;
+      for (int t = 0; t < K; ++t) {
+        // S_{t-1} k^_t over the row: the lane's columns, then the row's eight lanes (every lane of
+        // the row ends with the same sum: the butterfly adds the same pairs in each)
+        const float* kr = sY + t * L::SSTRIDE + col;
+        float4 kv[F];
+#pragma unroll
+        for (int f = 0; f < F; ++f) kv[f] = *reinterpret_cast<const float4*>(kr + 32 * f);
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int f = 0; f < F; ++f) {
+          a0 = __ffma2_rn(make_float2(s[f].x, s[f].y), make_float2(kv[f].x, kv[f].y), a0);
+          a1 = __ffma2_rn(make_float2(s[f].z, s[f].w), make_float2(kv[f].z, kv[f].w), a1);
+        }
+        float a = (a0.x + a0.y) + (a1.x + a1.y);
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        a += __shfl_xor_sync(0xffffffffu, a, 4);
+        const float g = sBG[kKMax + t];
+        const float u = sBG[t] * fmaf(-g, a, sV[t * kRows + row]);
+        // S_t = g S_{t-1} + u k^_t, stored straight from registers (the intermediates streaming,
+        // evict-first; the final state with the normal policy)
+        float* dst = (t == K - 1) ? fin : inter + size_t(t) * inter_stride;
+        const float2 gg = make_float2(g, g), uu = make_float2(u, u);
+#pragma unroll
+        for (int f = 0; f < F; ++f) {
+          const float2 lo = __ffma2_rn(uu, make_float2(kv[f].x, kv[f].y), __fmul2_rn(gg, make_float2(s[f].x, s[f].y)));
+          const float2 hi = __ffma2_rn(uu, make_float2(kv[f].z, kv[f].w), __fmul2_rn(gg, make_float2(s[f].z, s[f].w)));
+          s[f] = make_float4(lo.x, lo.y, hi.x, hi.y);
+          float4* d4 = reinterpret_cast<float4*>(dst + 32 * f);
+          if (t == K - 1)
+            *d4 = s[f];
+          else
+            __stcs(d4, s[f]);
+        }
+        // o_t = q_scale S_t q^_t
+        const float* qr = sY + (kKMax + t) * L::SSTRIDE + col;
+        float2 b0 = make_float2(0.f, 0.f), b1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int f = 0; f < F; ++f) {
+          const float4 qv = *reinterpret_cast<const float4*>(qr + 32 * f);
+          b0 = __ffma2_rn(make_float2(s[f].x, s[f].y), make_float2(qv.x, qv.y), b0);
+          b1 = __ffma2_rn(make_float2(s[f].z, s[f].w), make_float2(qv.z, qv.w), b1);
+        }
+        float o = (b0.x + b0.y) + (b1.x + b1.y);
+        o += __shfl_xor_sync(0xffffffffu, o, 1);
+        o += __shfl_xor_sync(0xffffffffu, o, 2);
+        o += __shfl_xor_sync(0xffffffffu, o, 4);
+        o *= p.q_scale;
+        if (t == cg) o_a = o;
+        if (t == cg + 8) o_b = o;
+      }
     }
     if constexpr (!kGated) {
 #pragma unroll
