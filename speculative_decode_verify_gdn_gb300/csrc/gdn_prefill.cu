@@ -1139,11 +1139,560 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state_kernel(con
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
+// ------------------------------------------------------------------------------------------
+// Kernel 2 at dv = 128: one CTA per (prompt, v-head), the whole 128-row state as one M = 128
+// accumulator (row m in TMEM lane m), so that every MMA does twice the work of an M = 64 one in
+// the same time and 256 CTAs make 2 waves where 512 made 4.  The operand space this needs is
+// found in tensor memory: the S operand's hi and lo halves live there as the A operand of the P
+// product (row m in lane m, two bf16 per 32-bit column), and P needs one buffer because the
+// epilogue turns its q^ half into the initial value Gamma o P_q of the o accumulator, onto which
+// the o' MMA then adds.  TMEM: the state (dk columns), P (128), u (64), o (64), S hi and lo
+// (dk / 2 each) - all 512 columns at dk = 128.  Epilogue warp w reaches lanes 32 (w % 4) ..
+// + 31 (rows) with the 32x32b shape; warps w and w + 4 split the columns.  Raw x is staged as
+// bf16 (it is bf16), the three history rows as f32.
+template <int DK>
+struct Tc128Layout {
+  static constexpr int ROWS = 128;
+  static constexpr int BLK_KQ = kCh * DK * 2;               // one 64 x DK bf16 operand
+  static constexpr int BLK_R = ROWS * kCh * 2;              // one 128 x 64 bf16 operand (r, d o u, u)
+  static constexpr int BLK = kCh * kCh * 2;                 // one 64 x 64 bf16 operand (W, MQ)
+  static constexpr int OFF_KH = 0;                          // [k^0 | q^ | k^1] hi
+  static constexpr int OFF_KL = OFF_KH + 3 * BLK_KQ;        // the same, lo
+  static constexpr int OFF_W = OFF_KL + 3 * BLK_KQ;         // W hi, lo
+  static constexpr int OFF_MQ = OFF_W + 2 * BLK;            // MQ hi, lo
+  static constexpr int OFF_GD = OFF_MQ + 2 * BLK;           // two buffers of Gamma[64], d[64]
+  static constexpr int OFF_RD = OFF_GD + 2 * 2 * kCh * 4;   // r hi, lo; later (d o u) hi, lo
+  static constexpr int OFF_U = OFF_RD + 2 * BLK_R;          // u hi, lo; later the staged outputs
+  static constexpr int OFF_H = OFF_U + 2 * BLK_R;           // three history rows [3][128] f32
+  static constexpr int OFF_X = OFF_H + 3 * ROWS * 4;        // raw x of a chunk [64][128] bf16
+  static constexpr int OFF_TAP = OFF_X + kCh * ROWS * 2;    // conv taps [128][4]
+  static constexpr int OFF_BAR = OFF_TAP + ROWS * 16;       // mbarriers
+  static constexpr int NBAR = 16;
+  static constexpr int OFF_TSLOT = OFF_BAR + NBAR * 8;
+  static constexpr int BYTES = OFF_TSLOT + 16;
+  static_assert(2 * BLK_R >= kCh * ROWS * 4, "the staged outputs fit in the u operand's space");
+  static_assert(OFF_X % 16 == 0 && OFF_TAP % 16 == 0 && OFF_BAR % 8 == 0, "alignment");
+  static_assert(BYTES <= 227 * 1024, "one CTA per SM");
+};
+
+// TMEM columns of the M = 128 kernel
+constexpr uint32_t kC8S = 0, kC8P = 128, kC8U = 256, kC8O = 320, kC8SH = 384, kC8SL = 448;
+// its extra mbarrier: the u operand written (the o' MMA waits for it; the update MMA, on the
+// chain, waits only for d o u)
+constexpr int kRdyUo = kNumBars;
+
+// Three-pass split product with the A operand in TMEM (hi and lo halves at a_hi, a_lo; a K step
+// of 16 is 8 columns) and the B operand K-major in shared memory.
+template <int KSTEPS>
+__device__ __forceinline__ void umma_split3_at(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hi, uint32_t b_lo,
+                                               uint32_t b_sbo, uint32_t idesc) {
+  const uint64_t dbh = umma_smem_desc(b_hi, 128, b_sbo), dbl = umma_smem_desc(b_lo, 128, b_sbo);
+#pragma unroll
+  for (int sp = 0; sp < 3; ++sp) {
+    const uint32_t a = (sp == 2) ? a_lo : a_hi;
+    const uint64_t db = (sp == 1) ? dbl : dbh;
+#pragma unroll
+    for (int kk = 0; kk < KSTEPS; ++kk) {
+      const uint32_t acc = (sp > 0 || kk > 0) ? 1u : 0u;
+      asm volatile(
+          "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+          "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+          "r"(a + 8 * kk), "l"(db + uint64_t(16 * kk)), "r"(idesc), "r"(acc)
+          : "memory");
+    }
+  }
+}
+
+// The staged output table [64 tokens][128 rows] f32: row (token) t, column c at t * 128 +
+// (c ^ sw) with the column bits 5-6 and the token's low bit folded into bits 2-4, so that both
+// the row-per-lane writes and the 16-byte reads of 32 columns per lane are free of conflicts.
+__device__ __forceinline__ int out_col(int t, int c) { return c ^ ((((c >> 5) & 3) | ((t & 1) << 2)) << 2); }
+
+template <int DK>
+__global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state128_kernel(const PrefillParams p) {
+  using L = Tc128Layout<DK>;
+  constexpr int ROWS = L::ROWS;
+  constexpr int SC = DK / 2;   // state columns per epilogue thread (two warps per lane quarter)
+  constexpr int SP = DK / 4;   // packed bf16 pairs of them
+  static_assert(SC == 32 || SC == 64, "dk = 64 or 128");
+  extern __shared__ __align__(128) uint8_t smb[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int i = blockIdx.y;
+  const int h = blockIdx.x;
+  const int kh = h / (p.Hv / p.Hk);
+  if (p.ws.meta[0] == 0) return;
+  const int32_t* base = p.ws.meta + 4;
+  const int c_first = base[i], n_chunks = base[i + 1] - base[i];
+  const long long s0 = p.cu[i], s1 = p.cu[i + 1];
+  const size_t C = size_t(p.C);
+  const size_t vch0 = size_t(2) * p.Hk * DK + size_t(h) * ROWS;  // first conv channel of the head
+  float* sH = reinterpret_cast<float*>(smb + L::OFF_H);
+  uint16_t* sX = reinterpret_cast<uint16_t*>(smb + L::OFF_X);
+  float* sTap = reinterpret_cast<float*>(smb + L::OFF_TAP);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smb + L::OFF_BAR);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smb + L::OFF_TSLOT);
+  const uint32_t sbase = smem_addr(smb);
+
+  // epilogue coordinates: row m = lane 32 quad + lane, column half hh (tokens 32 hh .. + 31 of a
+  // chunk, state columns hh SC .. + SC - 1)
+  const int quad = warp & 3, hh = warp >> 2;
+  const int m = 32 * quad + lane;
+  const bool epi = warp < kThreads / 32;
+  const uint32_t lane_sel = uint32_t(32 * quad) << 16;
+
+  static_assert(L::NBAR > kRdyUo, "mbarrier slots");
+  if (tid == 0) {
+    for (int q = 0; q <= kRdyUo; ++q) mbar_init(bar + q, q >= kRdyR ? kEpiThreads : 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(tslot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+
+  int armed[kNumBars] = {};
+  auto kq_src = [&](int c) {
+    return reinterpret_cast<const uint8_t*>(p.ws.kq) + (size_t(c) * p.Hk + kh) * kKqBlocks * L::BLK_KQ;
+  };
+  auto issue_k = [&](int c, int b) {
+    ++armed[kBarK0 + b];
+    mbar_arrive_expect_tx(bar + kBarK0 + b, 2 * L::BLK_KQ);
+    bulk_load(smb + L::OFF_KH + 2 * b * L::BLK_KQ, kq_src(c), L::BLK_KQ, bar + kBarK0 + b);
+    bulk_load(smb + L::OFF_KL + 2 * b * L::BLK_KQ, kq_src(c) + L::BLK_KQ, L::BLK_KQ, bar + kBarK0 + b);
+  };
+  auto issue_q = [&](int c) {
+    ++armed[kBarQ];
+    mbar_arrive_expect_tx(bar + kBarQ, 2 * L::BLK_KQ);
+    bulk_load(smb + L::OFF_KH + L::BLK_KQ, kq_src(c) + 2 * L::BLK_KQ, L::BLK_KQ, bar + kBarQ);
+    bulk_load(smb + L::OFF_KL + L::BLK_KQ, kq_src(c) + 3 * L::BLK_KQ, L::BLK_KQ, bar + kBarQ);
+  };
+  auto wq_src = [&](int c) {
+    return reinterpret_cast<const uint8_t*>(p.ws.wm) + (size_t(c) * p.Hv + h) * (4 * L::BLK);
+  };
+  auto issue_w = [&](int c) {
+    ++armed[kBarW];
+    mbar_arrive_expect_tx(bar + kBarW, 2 * L::BLK);
+    bulk_load(smb + L::OFF_W, wq_src(c), 2 * L::BLK, bar + kBarW);
+  };
+  auto issue_mq = [&](int c) {
+    ++armed[kBarMQ];
+    mbar_arrive_expect_tx(bar + kBarMQ, 2 * L::BLK);
+    bulk_load(smb + L::OFF_MQ, wq_src(c) + 2 * L::BLK, 2 * L::BLK, bar + kBarMQ);
+  };
+  auto issue_gd = [&](int lc) {  // buffer lc & 1 holds local chunk lc
+    const int b = lc & 1, c = c_first + lc;
+    ++armed[kBarGD0 + b];
+    mbar_arrive_expect_tx(bar + kBarGD0 + b, 2 * kCh * 4);
+    bulk_load(smb + L::OFF_GD + b * 2 * kCh * 4, p.ws.gd + (size_t(c) * p.Hv + h) * (2 * kCh), 2 * kCh * 4,
+              bar + kBarGD0 + b);
+  };
+  if (tid == kIssuer && n_chunks > 0) {
+    issue_k(c_first, 0);
+    issue_q(c_first);
+    issue_w(c_first);
+    issue_mq(c_first);
+    issue_gd(0);
+    if (n_chunks > 1) {
+      issue_gd(1);
+      issue_k(c_first + 1, 1);
+    }
+  }
+
+  // hi/lo operand stores of 32 consecutive K values (this thread's tokens) of row m of a K-major
+  // [128][64] operand (lo block BLK_R bytes after hi)
+  auto store_row32 = [&](int off, const float* v) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      uint4 hi, lo;
+      split8(v + 8 * g, hi, lo);
+      const uint32_t o = kmajor_off(m, 32 * hh + 8 * g, kCh);
+      *reinterpret_cast<uint4*>(smb + off + o) = hi;
+      *reinterpret_cast<uint4*>(smb + off + L::BLK_R + o) = lo;
+    }
+  };
+  // state columns hh SC + 32 q .. + 31 of this thread's row: loaded, stored, and split into the S
+  // operand (packed two per TMEM column), one 32-column slice at a time
+  auto ld_state = [&](int q, float (&sv)[32]) { tmem_ld32(tmem + lane_sel + kC8S + hh * SC + 32 * q, sv); };
+  auto st_state = [&](int q, const float (&sv)[32]) { tmem_st32(tmem + lane_sel + kC8S + hh * SC + 32 * q, sv); };
+  auto store_s_operand = [&](int q, const float (&sv)[32]) {
+    float ph[16], pl[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      uint32_t hi, lo;
+      split2(sv[2 * e], sv[2 * e + 1], hi, lo);
+      ph[e] = __uint_as_float(hi);
+      pl[e] = __uint_as_float(lo);
+    }
+    tmem_st16(tmem + lane_sel + kC8SH + hh * SP + 16 * q, ph);
+    tmem_st16(tmem + lane_sel + kC8SL + hh * SP + 16 * q, pl);
+  };
+
+  // the state into TMEM and, split, into the S operand; taps; the v channels' history
+  if (epi) {
+    const float* src = p.state_in + ((size_t(i) * p.Hv + h) * ROWS + m) * DK + hh * SC;
+#pragma unroll
+    for (int q = 0; q < SC / 32; ++q) {
+      float sv[32];
+#pragma unroll
+      for (int e = 0; e < 32; e += 4) {
+        const float4 f = *reinterpret_cast<const float4*>(src + 32 * q + e);
+        sv[e] = f.x;
+        sv[e + 1] = f.y;
+        sv[e + 2] = f.z;
+        sv[e + 3] = f.w;
+      }
+      st_state(q, sv);
+      store_s_operand(q, sv);
+    }
+  }
+  if (tid < ROWS) *reinterpret_cast<float4*>(sTap + 4 * tid) = *reinterpret_cast<const float4*>(p.conv_w + (vch0 + tid) * kConvW);
+  for (int idx = tid; idx < 3 * ROWS; idx += kThreads + 32) {
+    const int mm = idx / ROWS, ch = idx % ROWS;
+    sH[idx] = p.conv_state_in[(size_t(i) * 3 + mm) * C + vch0 + ch];
+  }
+  // raw x of the head's 128 channels for one chunk: thread = (token tid / 4, 32 channels)
+  const int xt = tid >> 2, xg = tid & 3;
+  uint4 xr[4] = {};
+  if (epi && n_chunks > 0 && xt < min_ll(kCh, s1 - s0)) {
+    const uint4* src = reinterpret_cast<const uint4*>(p.x + size_t(s0 + xt) * C + vch0 + 32 * xg);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) xr[q] = src[q];
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  const uint32_t id_n64 = umma_idesc_bf16(ROWS, kCh);
+  const uint32_t id_n128 = umma_idesc_bf16(ROWS, 2 * kCh);
+  const uint32_t id_ndk_bmn = umma_idesc_bf16(ROWS, DK) | (1u << 16);  // B MN-major
+  bool failed = false;
+  if (n_chunks > 0) {
+    // the state in TMEM is kept pre-scaled by the current chunk's Gamma_63, so that the update
+    // MMA can accumulate onto it (the S operand holds it unscaled)
+    if (wait_failed(bar + kBarGD0, 0)) {
+      failed = true;
+    } else {
+      tc_fence_after();
+      if (epi) {
+        const float gl = reinterpret_cast<const float*>(smb + L::OFF_GD)[kCh - 1];
+#pragma unroll
+        for (int q = 0; q < SC / 32; ++q) {
+          float sv[32];
+          ld_state(q, sv);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sv[e] *= gl;
+          st_state(q, sv);
+        }
+      }
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+    }
+  }
+
+  int len = 0;
+  if (tid == kIssuer) {
+    for (int lc = 0; lc < n_chunks && !failed; ++lc) {
+      const uint32_t par = lc & 1;
+      const bool more = lc + 1 < n_chunks;
+      // P = S [k^ | q^]^T with S from TMEM, once the S operand is written (and the previous
+      // chunk's P has been read: the same hand-over); [k^0 | q^] for even chunks, P_k in the
+      // first 64 columns, [q^ | k^1] for odd ones, P_k in the second 64
+      if ((lc > 0 && !mbar_wait_bounded(bar + kRdyS, (lc - 1) & 1)) ||
+          !mbar_wait_bounded(bar + kBarK0 + par, (lc >> 1) & 1) || !mbar_wait_bounded(bar + kBarQ, par)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      {
+        const uint32_t bo = (par ? 1 : 0) * L::BLK_KQ;
+        umma_split3_at<DK / 16>(tmem + kC8P, tmem + kC8SH, tmem + kC8SL, sbase + L::OFF_KH + bo,
+                                sbase + L::OFF_KL + bo, (DK / 8) * 128, id_n128);
+        umma_commit(bar + kBarPk);
+        ++armed[kBarPk];
+      }
+      // copies only right after an MMA group: this chunk's MQ, the next chunk's k^
+      if (lc > 0) {
+        if (!mbar_wait_bounded(bar + kBarO, (lc - 1) & 1)) {
+          failed = true;
+          break;
+        }
+        issue_mq(c_first + lc);
+        if (more) {
+          if (!mbar_wait_bounded(bar + kBarS, (lc - 1) & 1)) {
+            failed = true;
+            break;
+          }
+          issue_k(c_first + lc + 1, (lc + 1) & 1);
+        }
+      }
+      // u = r W^T; then the next chunk's q^
+      if (!mbar_wait_bounded(bar + kRdyR, par) || !mbar_wait_bounded(bar + kBarW, par)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      umma_split3<kCh / 16>(tmem + kC8U, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK_R, sbase + L::OFF_W,
+                            sbase + L::OFF_W + L::BLK, 1024, id_n64, false);
+      umma_commit(bar + kBarU);
+      ++armed[kBarU];
+      if (more) issue_q(c_first + lc + 1);
+      // S += (d o u) k^, then o += u MQ^T (onto Gamma o P_q); then the next W and Gamma, d
+      if (!mbar_wait_bounded(bar + kRdyU, par)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      umma_split3_bmn<kCh / 16>(tmem + kC8S, sbase + L::OFF_RD, sbase + L::OFF_RD + L::BLK_R, 1024,
+                                sbase + L::OFF_KH + 2 * par * L::BLK_KQ, sbase + L::OFF_KL + 2 * par * L::BLK_KQ,
+                                (DK / 8) * 128, 128, id_ndk_bmn, true);
+      umma_commit(bar + kBarS);
+      ++armed[kBarS];
+      if (!mbar_wait_bounded(bar + kBarMQ, par) || !mbar_wait_bounded(bar + kRdyUo, par)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      umma_split3<kCh / 16>(tmem + kC8O, sbase + L::OFF_U, sbase + L::OFF_U + L::BLK_R, sbase + L::OFF_MQ,
+                            sbase + L::OFF_MQ + L::BLK, 1024, id_n64, true);
+      umma_commit(bar + kBarO);
+      ++armed[kBarO];
+      if (more) issue_w(c_first + lc + 1);
+      if (lc + 2 < n_chunks) issue_gd(lc + 2);
+    }
+  } else if (epi && !failed && n_chunks > 0) {
+    // raw x of a chunk into the staging table (zero past the prompt's end), then the next
+    // chunk's x is fetched
+    auto stage_x = [&](long long tok0, int n) {
+      uint4* dst = reinterpret_cast<uint4*>(sX + xt * ROWS + 32 * xg);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = (xt < n) ? xr[q] : make_uint4(0, 0, 0, 0);
+      const long long nt = tok0 + kCh + xt;
+      if (nt < s1) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.x + size_t(nt) * C + vch0 + 32 * xg);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) xr[q] = src[q];
+      }
+    };
+    // value idx of the chunk's window [history rows 0..2, x_0 .. x_63] for channel m
+    auto win = [&](int idx) { return idx < 3 ? sH[idx * ROWS + m] : bf16_to_f32(sX[(idx - 3) * ROWS + m]); };
+    // conv + SiLU of channel m at this thread's 32 tokens
+    float v[32];
+    auto conv = [&]() {
+      const float4 w = *reinterpret_cast<const float4*>(sTap + 4 * m);
+      float a0 = win(32 * hh), a1 = win(32 * hh + 1), a2 = win(32 * hh + 2);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float a3 = win(32 * hh + j + 3);
+        v[j] = silu(fmaf(w.w, a3, fmaf(w.z, a2, fmaf(w.y, a1, w.x * a0))));
+        a0 = a1;
+        a1 = a2;
+        a2 = a3;
+      }
+    };
+    float* sOut = reinterpret_cast<float*>(smb + L::OFF_U);  // [64 tokens][128 rows], out_col order
+    auto hand_over = [&](uint64_t* rdy) {
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(rdy);
+    };
+
+    stage_x(s0, int(min_ll(kCh, s1 - s0)));
+    epi_sync();
+    conv();
+    for (int lc = 0; lc < n_chunks; ++lc) {
+      const uint32_t par = lc & 1;
+      const float* sGam = reinterpret_cast<const float*>(smb + L::OFF_GD + (lc & 1) * 2 * kCh * 4);
+      const float* sd = sGam + kCh;
+      const long long tok0 = s0 + (long long)lc * kCh;
+      len = int(min_ll(kCh, s1 - tok0));
+      const bool more = lc + 1 < n_chunks;
+
+      // (a) r = v - Gamma o P_k -> operand (on the chain); then o = Gamma o P_q into the o
+      // accumulator (the o' MMA adds onto it) and the last three raw rows become the next
+      // chunk's history
+      if (epi_any(!mbar_wait_bounded(bar + kBarPk, par))) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      {
+        float pk[32];
+        tmem_ld32(tmem + lane_sel + kC8P + (par ? kCh : 0) + 32 * hh, pk);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pk[j] = fmaf(-sGam[32 * hh + j], pk[j], v[j]);
+        store_row32(L::OFF_RD, pk);
+      }
+      hand_over(bar + kRdyR);
+      {
+        float pq[32];
+        tmem_ld32(tmem + lane_sel + kC8P + (par ? 0 : kCh) + 32 * hh, pq);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) pq[j] *= sGam[32 * hh + j];
+        tmem_st32(tmem + lane_sel + kC8O + 32 * hh, pq);
+      }
+      if (len == kCh) {
+        for (int idx = tid; idx < 3 * ROWS; idx += kThreads) sH[idx] = bf16_to_f32(sX[(kCh - 3) * ROWS + idx]);
+      }
+      // (b) d o u -> the update's operand (on the chain), then u -> the o' MMA's
+      if (epi_any(!mbar_wait_bounded(bar + kBarU, par))) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      {
+        float u[32], du[32];
+        tmem_ld32(tmem + lane_sel + kC8U + 32 * hh, u);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) du[j] = u[j] * sd[32 * hh + j];
+        store_row32(L::OFF_RD, du);  // r is dead: the u MMAs are done
+        hand_over(bar + kRdyU);
+        store_row32(L::OFF_U, u);
+      }
+      hand_over(bar + kRdyUo);
+      // (c) while the state update runs: the next chunk's raw x and conv
+      if (more) {
+        stage_x(tok0 + kCh, int(min_ll(kCh, s1 - tok0 - kCh)));
+        epi_sync();
+        conv();
+      }
+      // (d) the new state: split into the S operand of the next chunk (unscaled), and pre-scaled
+      // in TMEM by the next chunk's Gamma_63
+      {
+        bool ok = mbar_wait_bounded(bar + kBarS, par);
+        if (more) ok = ok && mbar_wait_bounded(bar + kBarGD0 + ((lc + 1) & 1), ((lc + 1) >> 1) & 1);
+        if (epi_any(!ok)) {
+          failed = true;
+          break;
+        }
+      }
+      tc_fence_after();
+      // (the S operand first: the next P waits for it; the update that adds onto the re-scaled
+      // state is issued only after this chunk's hand-overs)
+      if (more) {
+#pragma unroll
+        for (int q = 0; q < SC / 32; ++q) {
+          float sv[32];
+          ld_state(q, sv);
+          store_s_operand(q, sv);
+        }
+      }
+      hand_over(bar + kRdyS);
+      if (more) {
+        const float gl = reinterpret_cast<const float*>(smb + L::OFF_GD + ((lc + 1) & 1) * 2 * kCh * 4)[kCh - 1];
+#pragma unroll
+        for (int q = 0; q < SC / 32; ++q) {
+          float sv[32];
+          ld_state(q, sv);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sv[e] *= gl;
+          st_state(q, sv);
+        }
+      }
+      // (e) this chunk's outputs, while the next chunk's P runs: o = q_scale (Gamma o P_q + o'),
+      // staged token-major in the u operand's space (the o' MMAs are done with it), then
+      // written out as 16-byte stores, thread = (token xt, 32 rows)
+      if (epi_any(!mbar_wait_bounded(bar + kBarO, par))) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      {
+        float o[32];
+        tmem_ld32(tmem + lane_sel + kC8O + 32 * hh, o);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int t = 32 * hh + j;
+          sOut[t * ROWS + out_col(t, m)] = p.q_scale * o[j];
+        }
+      }
+      epi_sync();
+      if (xt < len) {
+        const float* src = sOut + xt * ROWS;
+        const size_t oi = size_t(tok0 + xt) * p.Hv * ROWS + size_t(h) * ROWS + 32 * xg;
+        float4 f[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) f[q] = *reinterpret_cast<const float4*>(src + out_col(xt, 32 * xg + 4 * q));
+        if (p.out_f32) {
+          float4* o4 = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) o4[q] = f[q];
+        } else {
+          uint32_t w[16];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const __nv_bfloat162 b0 = __floats2bfloat162_rn(f[q].x, f[q].y);
+            const __nv_bfloat162 b1 = __floats2bfloat162_rn(f[q].z, f[q].w);
+            w[2 * q] = *reinterpret_cast<const uint32_t*>(&b0);
+            w[2 * q + 1] = *reinterpret_cast<const uint32_t*>(&b1);
+          }
+          uint4* o4 = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + oi);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) o4[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        }
+      }
+      // (the staging space is next written as the u operand in (b), behind the barrier of (a))
+    }
+  }
+  __syncwarp();
+  failed = __syncthreads_or(failed) != 0;
+
+  if (failed) {
+    if (tid == kIssuer) {  // every copy and MMA group still in flight lands before TMEM is freed
+      atomicOr(p.err, kDevErrTimeout);
+      for (int q = 0; q < kNumBars; ++q)
+        if (armed[q] > 0) (void)mbar_drain(bar + q, uint32_t(armed[q] - 1) & 1u);
+    }
+  } else {
+    // final state from TMEM (the last update left it unscaled)
+    if (epi) {
+      float* dst = p.state_out + ((size_t(i) * p.Hv + h) * ROWS + m) * DK + hh * SC;
+#pragma unroll
+      for (int q = 0; q < SC / 32; ++q) {
+        float sv[32];
+        ld_state(q, sv);
+#pragma unroll
+        for (int e = 0; e < 32; e += 4)
+          *reinterpret_cast<float4*>(dst + 32 * q + e) = make_float4(sv[e], sv[e + 1], sv[e + 2], sv[e + 3]);
+      }
+    }
+    // conv history: the v channels from window rows len .. len + 2 of the last chunk (the
+    // untouched history of an empty prompt)
+    for (int idx = tid; epi && idx < 3 * ROWS; idx += kThreads) {  // (epilogue threads know len)
+      const int mm = idx / ROWS, ch = idx % ROWS, row = len + mm;
+      p.conv_state_out[(size_t(i) * 3 + mm) * C + vch0 + ch] =
+          row < 3 ? sH[row * ROWS + ch] : bf16_to_f32(sX[(row - 3) * ROWS + ch]);
+    }
+    // the q|k channels of the head group, by the group's first v-head; every value is read
+    // before this thread writes, and no other thread of this grid reads them
+    if (h % (p.Hv / p.Hk) == 0) {
+      for (int q = tid; q < 2 * DK; q += kThreads + 32) {
+        const size_t gch = (q < DK) ? size_t(kh) * DK + q : size_t(p.Hk) * DK + size_t(kh) * DK + (q - DK);
+        float hv[3];
+#pragma unroll
+        for (int mm = 0; mm < 3; ++mm) {
+          const long long pos = s1 - 3 + mm;
+          hv[mm] = (pos >= s0) ? bf16_to_f32(p.x[size_t(pos) * C + gch])
+                               : p.conv_state_in[(size_t(i) * 3 + size_t(pos - s0 + 3)) * C + gch];
+        }
+#pragma unroll
+        for (int mm = 0; mm < 3; ++mm) p.conv_state_out[(size_t(i) * 3 + mm) * C + gch] = hv[mm];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
 template <int DK, int DV>
 cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   auto k1 = gdn_prefill_chunk_kernel<DK>;
-  auto k2 = gdn_prefill_state_kernel<DK, DV>;
-  const size_t b1 = ChunkLayout<DK>::BYTES, b2 = TcLayout<DK>::BYTES;
+  // dv = 128: the whole v-head per CTA (M = 128); dv = 64: the M = 64 kernel, also one CTA per head
+  constexpr bool kM128 = DV == 128;
+  auto k2 = kM128 ? gdn_prefill_state128_kernel<DK> : gdn_prefill_state_kernel<DK, DV>;
+  const size_t b1 = ChunkLayout<DK>::BYTES, b2 = kM128 ? size_t(Tc128Layout<DK>::BYTES) : size_t(TcLayout<DK>::BYTES);
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, int(b1));
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, int(b2));
@@ -1154,7 +1703,7 @@ cudaError_t launch_prefill_t(const PrefillParams& p, cudaStream_t stream) {
   k1<<<dim3(unsigned(p.ws.chunk_cap), unsigned(p.Hk), 1), kThreads, b1, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  k2<<<dim3(unsigned(p.Hv * (DV / kTileRows)), unsigned(p.B), 1), kThreads + 32, b2, stream>>>(p);
+  k2<<<dim3(unsigned(p.Hv * (kM128 ? 1 : DV / kTileRows)), unsigned(p.B), 1), kThreads + 32, b2, stream>>>(p);
   return cudaGetLastError();
 }
 
