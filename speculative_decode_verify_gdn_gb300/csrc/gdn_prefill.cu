@@ -1351,14 +1351,18 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state128_kernel(
     const int mm = idx / ROWS, ch = idx % ROWS;
     sH[idx] = p.conv_state_in[(size_t(i) * 3 + mm) * C + vch0 + ch];
   }
-  // raw x of the head's 128 channels for one chunk: thread = (token tid / 4, 32 channels)
-  const int xt = tid >> 2, xg = tid & 3;
+  // raw x of the head's 128 channels for one chunk: thread = (channels 8 xc .. + 7, tokens
+  // xr0 + 16 q), so that each quarter-warp's 16-byte stores fill 128 contiguous bytes of a row
+  const int xc = tid & 15, xr0 = (tid >> 4) & 15;
   uint4 xr[4] = {};
-  if (epi && n_chunks > 0 && xt < min_ll(kCh, s1 - s0)) {
-    const uint4* src = reinterpret_cast<const uint4*>(p.x + size_t(s0 + xt) * C + vch0 + 32 * xg);
+  if (epi && n_chunks > 0) {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) xr[q] = src[q];
+    for (int q = 0; q < 4; ++q)
+      if (xr0 + 16 * q < min_ll(kCh, s1 - s0))
+        xr[q] = *reinterpret_cast<const uint4*>(p.x + size_t(s0 + xr0 + 16 * q) * C + vch0 + 8 * xc);
   }
+  // the output write-out: thread = (token xt, rows 32 xg .. + 31)
+  const int xt = tid >> 2, xg = tid & 3;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -1465,14 +1469,12 @@ __global__ void __launch_bounds__(kThreads + 32, 1) gdn_prefill_state128_kernel(
     // raw x of a chunk into the staging table (zero past the prompt's end), then the next
     // chunk's x is fetched
     auto stage_x = [&](long long tok0, int n) {
-      uint4* dst = reinterpret_cast<uint4*>(sX + xt * ROWS + 32 * xg);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = (xt < n) ? xr[q] : make_uint4(0, 0, 0, 0);
-      const long long nt = tok0 + kCh + xt;
-      if (nt < s1) {
-        const uint4* src = reinterpret_cast<const uint4*>(p.x + size_t(nt) * C + vch0 + 32 * xg);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) xr[q] = src[q];
+      for (int q = 0; q < 4; ++q) {
+        const int t = xr0 + 16 * q;
+        *reinterpret_cast<uint4*>(sX + t * ROWS + 8 * xc) = (t < n) ? xr[q] : make_uint4(0, 0, 0, 0);
+        const long long nt = tok0 + kCh + t;
+        if (nt < s1) xr[q] = *reinterpret_cast<const uint4*>(p.x + size_t(nt) * C + vch0 + 8 * xc);
       }
     };
     // value idx of the chunk's window [history rows 0..2, x_0 .. x_63] for channel m
