@@ -399,20 +399,33 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
     // (thread 64).  Every factor is in [0, 1]: nothing overflows, nothing cancels (a difference
     // of running sums of log g would lose digits once those sums are large, and gives NaN after
     // a token with g = 0), and a product that underflows is below anything it is added to.
-    if (gt < kCh) {
-      const int j = gt;
-      float d = 1.f;
-#pragma unroll 8
-      for (int t = 0; t < kCh; ++t) {
-        if (t > j) d *= sG[t];
-        sD[t * kAS + j] = (t < j) ? 0.f : d;
+    // (the g values come in as sixteen 16-byte broadcasts before the products, so that the chain
+    // of 64 multiplies does not wait on a shared-memory load at every step)
+    if (gt <= kCh) {
+      float gv[kCh];
+#pragma unroll
+      for (int t = 0; t < kCh; t += 4) {
+        const float4 q4 = *reinterpret_cast<const float4*>(sG + t);
+        gv[t] = q4.x;
+        gv[t + 1] = q4.y;
+        gv[t + 2] = q4.z;
+        gv[t + 3] = q4.w;
       }
-    } else if (gt == kCh) {
-      float gam = 1.f;
-#pragma unroll 8
-      for (int t = 0; t < kCh; ++t) {
-        gam *= sG[t];
-        sGam[t] = gam;
+      if (gt < kCh) {
+        const int j = gt;
+        float d = 1.f;
+#pragma unroll
+        for (int t = 0; t < kCh; ++t) {
+          if (t > j) d *= gv[t];
+          sD[t * kAS + j] = (t < j) ? 0.f : d;
+        }
+      } else {
+        float gam = 1.f;
+#pragma unroll
+        for (int t = 0; t < kCh; ++t) {
+          gam *= gv[t];
+          sGam[t] = gam;
+        }
       }
     }
     gsync();
