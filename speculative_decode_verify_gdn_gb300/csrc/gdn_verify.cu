@@ -340,6 +340,32 @@ __device__ __forceinline__ float reduce4(const float (&p)[4], int lane) {
   return k;
 }
 
+// Two reduce4 at once, their shuffles interleaved (the sums and their order are reduce4's).
+__device__ __forceinline__ void reduce4_pair(const float (&p)[4], const float (&q)[4], int lane, float& rp,
+                                             float& rq) {
+  const bool h16 = (lane & 16) != 0, h8 = (lane & 8) != 0;
+  float k0 = h16 ? p[2] : p[0], k1 = h16 ? p[3] : p[1];
+  float m0 = h16 ? q[2] : q[0], m1 = h16 ? q[3] : q[1];
+  const float x0 = h16 ? p[0] : p[2], x1 = h16 ? p[1] : p[3];
+  const float y0 = h16 ? q[0] : q[2], y1 = h16 ? q[1] : q[3];
+  k0 += __shfl_xor_sync(0xffffffffu, x0, 16);
+  m0 += __shfl_xor_sync(0xffffffffu, y0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, x1, 16);
+  m1 += __shfl_xor_sync(0xffffffffu, y1, 16);
+  float k = h8 ? k1 : k0, mm = h8 ? m1 : m0;
+  const float x = h8 ? k0 : k1, y = h8 ? m0 : m1;
+  k += __shfl_xor_sync(0xffffffffu, x, 8);
+  mm += __shfl_xor_sync(0xffffffffu, y, 8);
+  k += __shfl_xor_sync(0xffffffffu, k, 4);
+  mm += __shfl_xor_sync(0xffffffffu, mm, 4);
+  k += __shfl_xor_sync(0xffffffffu, k, 2);
+  mm += __shfl_xor_sync(0xffffffffu, mm, 2);
+  k += __shfl_xor_sync(0xffffffffu, k, 1);
+  mm += __shfl_xor_sync(0xffffffffu, mm, 1);
+  rp = k;
+  rq = mm;
+}
+
 // ------------------------------------------------------------------------------------------
 // Kernel 2: the q|k channels' history snapshots and new history (thread = channel pair 2i, 2i+1
 // of the 2 Hk dk q|k channels, q first).  Snapshot t of a chain window is the history after token
@@ -596,6 +622,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyPar
       float* inter = p.state_inter
                          ? p.state_inter + size_t(b) * (K - 1) * inter_stride + (size_t(h) * DV + r0) * DK + my_off
                          : nullptr;
+      float pq[kRowsPerWarp] = {0.f, 0.f, 0.f, 0.f};
       for (int t = 0; t < K; ++t) {
         // a node that does not continue the previous one starts from its parent's state, rebuilt
         // in its closed form S_par = Gamma_par S0 + sum_{j in path(par)} D[par][j] u_j k^_j^T
@@ -626,13 +653,22 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyPar
             for (int e = 0; e < V; ++e) s[r][e] = fmaf(d, sv[e], s[r][e]);
           }
         }
-        // S_{t-1} k^_t for the four rows (every lane ends with the same four sums)
+        // S_{t-1} k^_t for the four rows (every lane ends with the same four sums), reduced
+        // together with node t - 1's outputs (pq: their unreduced partials), so that the two
+        // reductions' shuffles hide each other's latency (seeded 16-node trees at the serving
+        // shape: 212.4 -> 203.7 us per step)
         float kv[V];
         load_vec<V>(sY + t * L::SSTRIDE + col, kv);
         float pk[kRowsPerWarp];
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) pk[r] = dot_vec<V>(s[r], kv);
-        const float a_m = reduce4(pk, lane);
+        float a_m, o_m;
+        reduce4_pair(pk, pq, lane, a_m, o_m);
+        if (t > 0) {
+          const float o = o_m * p.q_scale;
+          if (t - 1 == cg) o_a = o;
+          if (t - 1 == cg + 8) o_b = o;
+        }
         const float g = sBG[kKMax + t];
         const float beta = sBG[t];
         const float4 v4 = *reinterpret_cast<const float4*>(sV + t * kRows + row0);
@@ -651,15 +687,16 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyPar
           update_vec<V>(s[r], g, u[r], kv);
           store_vec<V>(dst + r * DK, s[r], t == K - 1);
         }
-        // o_t = q_scale S_t q^_t
+        // o_t = q_scale S_t q^_t: the lane's parts now, the sums with the next node's
         float qv[V];
         load_vec<V>(sY + (kKMax + t) * L::SSTRIDE + col, qv);
-        float pq[kRowsPerWarp];
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) pq[r] = dot_vec<V>(s[r], qv);
+      }
+      {
         const float o = reduce4(pq, lane) * p.q_scale;
-        if (t == cg) o_a = o;
-        if (t == cg + 8) o_b = o;
+        if (K - 1 == cg) o_a = o;
+        if (K - 1 == cg + 8) o_b = o;
       }
     } else {
       constexpr int F = DK / 32;
