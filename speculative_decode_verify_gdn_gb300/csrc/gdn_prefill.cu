@@ -15,10 +15,12 @@
 //   gdn_prefill_chunk_kernel   one CTA per (chunk, q/k head), all chunks in parallel: conv of the
 //                              q|k channels, L2 norms, Gram products, gates, decay products and
 //                              the 64 x 64 triangular inverse of every v-head of the group;
-//   gdn_prefill_state_kernel   one CTA per (prompt, v-head, 64 state rows): walks the prompt's
+//   gdn_prefill_state128_kernel (dv = 128) one CTA per (prompt, v-head), the whole state as one
+//                              M = 128 tile; gdn_prefill_state_kernel (dv = 64) one CTA per
+//                              (prompt, v-head, 64 state rows), M = 64: both walk the prompt's
 //                              chunks in order on the tensor cores with the state in tensor
 //                              memory, the next chunk's operands arriving by bulk copy while the
-//                              current one is computed; convolves its own v channels.
+//                              current one is computed, and convolve their own v channels.
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 
