@@ -465,9 +465,12 @@ struct VerifyLayout {
   static_assert(OFF_X % 2 == 0, "float2 scratch and exchange slots 8-byte aligned");
 };
 
-template <int DK, int DV, bool kTree, bool kGated>
+// kOne: the K = 1 instantiation (plain decode), with the window length fixed at compile time; the
+// token loop then has no previous output whose row sum to overlap with the next token's.
+template <int DK, int DV, bool kTree, bool kGated, bool kOne>
 __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyParams p) {
   static_assert(!(kTree && kGated), "tree and gated-norm variants are separate");
+  static_assert(!(kTree && kOne), "a one-node tree takes the tree variant");
   static_assert(DK == 64 || DK == 128, "dk = 64 or 128");
   using L = VerifyLayout<DK, DV, kTree, kGated>;
   constexpr int kTiles = L::kTiles;
@@ -483,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyPar
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int K = p.K;
+  const int K = kOne ? 1 : p.K;
   const int b = blockIdx.y;
   const int h = blockIdx.x / kTiles;
   const int r0 = (blockIdx.x % kTiles) * kRows;
@@ -737,11 +740,11 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyPar
         }
         float a = (a0.x + a0.y) + (a1.x + a1.y);
         a += __shfl_xor_sync(0xffffffffu, a, 1);
-        op += __shfl_xor_sync(0xffffffffu, op, 1);
+        if constexpr (!kOne) op += __shfl_xor_sync(0xffffffffu, op, 1);
         a += __shfl_xor_sync(0xffffffffu, a, 2);
-        op += __shfl_xor_sync(0xffffffffu, op, 2);
+        if constexpr (!kOne) op += __shfl_xor_sync(0xffffffffu, op, 2);
         a += __shfl_xor_sync(0xffffffffu, a, 4);
-        op += __shfl_xor_sync(0xffffffffu, op, 4);
+        if constexpr (!kOne) op += __shfl_xor_sync(0xffffffffu, op, 4);
         if (t > 0) keep_o(t - 1, op);
         const float g = sBG[kKMax + t];
         const float u = sBG[t] * fmaf(-g, a, sV[t * kRows + row]);
@@ -850,9 +853,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyPar
   }
 }
 
-template <int DK, int DV, bool kTree, bool kGated>
+template <int DK, int DV, bool kTree, bool kGated, bool kOne>
 cudaError_t launch_t(const VerifyParams& p, cudaStream_t stream) {
-  auto k1 = gdn_verify_kernel<DK, DV, kTree, kGated>;
+  auto k1 = gdn_verify_kernel<DK, DV, kTree, kGated, kOne>;
   const size_t b1 = VerifyLayout<DK, DV, kTree, kGated>::BYTES;
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, int(b1));
   if (e != cudaSuccess) return e;
@@ -894,9 +897,12 @@ cudaError_t launch_verify(const VerifyParams& p, cudaStream_t stream) {
   const bool gated = p.z != nullptr;
 #define GDN_LAUNCH(DK_, DV_)                                          \
   if (p.dk == DK_ && p.dv == DV_) {                                   \
-    if (gated) return launch_t<DK_, DV_, false, true>(p, stream);     \
-    if (tree) return launch_t<DK_, DV_, true, false>(p, stream);      \
-    return launch_t<DK_, DV_, false, false>(p, stream);               \
+    if (tree) return launch_t<DK_, DV_, true, false, false>(p, stream); \
+    if (p.K == 1)                                                       \
+      return gated ? launch_t<DK_, DV_, false, true, true>(p, stream)   \
+                   : launch_t<DK_, DV_, false, false, true>(p, stream); \
+    return gated ? launch_t<DK_, DV_, false, true, false>(p, stream)    \
+                 : launch_t<DK_, DV_, false, false, false>(p, stream);  \
   }
   GDN_LAUNCH(128, 128)
   GDN_LAUNCH(128, 64)

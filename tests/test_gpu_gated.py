@@ -101,6 +101,24 @@ def test_states_and_history_equal_plain_verify_bitwise():
         assert torch.equal(a, b)
 
 
+def test_decode_step_equals_first_token_of_a_window():
+    """The one-token instantiation of the gated variant against a two-token window's first
+    token, bit for bit (outputs after the norm, state and conv history)."""
+    d2 = Dims(B=3, K=2, Hk=2, Hv=8, dk=128, dv=128)
+    d1 = Dims(B=3, K=1, Hk=2, Hv=8, dk=128, dv=128)
+    g = Gen(4200)
+    lay = make_layer(g, d2, Dists())
+    rnd = make_round(g, d2, Dists())
+    one = Round(x=rnd.x[:, :1].copy(), a=rnd.a[:, :1].copy(), b=rnd.b[:, :1].copy(),
+                accept_len=np.ones(d1.B, np.int32))
+    z_bits, w = make_output_gate(g, d2)
+    win = _run_gated(d2, lay, rnd, z_bits, w, 1e-6)
+    dec = _run_gated(d1, lay, one, np.ascontiguousarray(z_bits[:, :1]), w, 1e-6)
+    assert torch.equal(dec.out[:, 0], win.out[:, 0])
+    assert torch.equal(dec.states[0], win.state_inter[:, 0])
+    assert torch.equal(dec.conv_states[0], win.conv_inter[:, 0])
+
+
 def test_serving_shape_sampled_sequences():
     """B=32, K=16, Hv=32 (the K=16 serving shape, cluster of 4 row tiles per head): sampled
     sequences against the oracle run on those sequences alone."""

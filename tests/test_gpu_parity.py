@@ -15,8 +15,8 @@ from parity_util import (OUT_TOL, OUT_TOL_BF16, STATE_TOL, bf16_tensor_to_f32, o
 from speculative_decode_verify_gdn_gb300 import gdn
 from speculative_decode_verify_gdn_gb300.build import build_library
 from speculative_decode_verify_gdn_gb300.runtime import GdnLayerState
-from speculative_decode_verify_gdn_gb300.synth import (WORKLOADS, Dims, Dists, Gen, bf16_bits_to_f32, make_layer,
-                                                        make_round)
+from speculative_decode_verify_gdn_gb300.synth import (WORKLOADS, Dims, Dists, Gen, Round, bf16_bits_to_f32,
+                                                        make_layer, make_round)
 
 pytestmark = pytest.mark.gpu
 
@@ -271,9 +271,10 @@ def test_dflash_workload_200_rounds_rollback_resume():
             np.testing.assert_array_equal(st.conv_state.cpu().numpy(), H)
 
 
-@pytest.mark.parametrize("name,rounds", [("dspark", 3), ("serve16", 2)])
+@pytest.mark.parametrize("name,rounds", [("decode", 4), ("dspark", 3), ("serve16", 2)])
 def test_batched_workloads_full_outputs(name, rounds):
-    """B=32 (K=8 and K=16), per-sequence rollback, every output compared."""
+    """Plain decode (B=1, K=1) and B=32 (K=8 and K=16), per-sequence rollback, every output
+    compared."""
     w = WORKLOADS[name]
     d = w.dims
     g = Gen(w.seed)
@@ -291,6 +292,33 @@ def test_batched_workloads_full_outputs(name, rounds):
         assert state_rel_err(st.state.cpu().numpy(), S) <= STATE_TOL
         np.testing.assert_array_equal(st.conv_state.cpu().numpy(), H)
         del ref
+
+
+@pytest.mark.parametrize("dk,dv", [(128, 128), (64, 128), (128, 64), (64, 64)])
+def test_decode_step_equals_first_token_of_a_window(dk, dv):
+    """A one-token call runs its own kernel instantiation (the window length fixed at compile
+    time); the recurrence is the same, so it gives, bit for bit, what a two-token window gives
+    for its first token: the output, the state after the token and the conv history after it."""
+    d2 = Dims(B=5, K=2, Hk=4, Hv=8, dk=dk, dv=dv)
+    d1 = Dims(B=5, K=1, Hk=4, Hv=8, dk=dk, dv=dv)
+    g = Gen(4100 + dk + dv)
+    lay = make_layer(g, d2, Dists())
+    rnd = make_round(g, d2, Dists())
+    one = Round(x=rnd.x[:, :1].copy(), a=rnd.a[:, :1].copy(), b=rnd.b[:, :1].copy(),
+                accept_len=np.ones(d1.B, np.int32))
+    win = GdnLayerState.create(d2, lay)
+    win.load_round(rnd)
+    win.verify()
+    dec = GdnLayerState.create(d1, lay)
+    dec.load_round(one)
+    dec.verify()
+    torch.cuda.synchronize()
+    assert torch.equal(dec.out[:, 0], win.out[:, 0])
+    assert torch.equal(dec.states[0], win.state_inter[:, 0])
+    assert torch.equal(dec.conv_states[0], win.conv_inter[:, 0])
+    assert torch.equal(dec.conv_inter[:, 0], win.conv_inter[:, 0])
+    ref = oracle_round(d1, lay, lay.state.astype(np.float64), lay.conv_state.astype(np.float64), one)
+    _check_round(dec, ref, d1)
 
 
 def test_stack48_workload_sampled_layers():
