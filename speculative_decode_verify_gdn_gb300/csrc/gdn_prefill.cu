@@ -31,10 +31,13 @@ __device__ __forceinline__ long long min_ll(long long a, long long b) { return a
 
 constexpr int kThreads = 256;
 constexpr int kCh = kPrefillChunk;   // 64 tokens per chunk
-constexpr int kAS = kCh + 1;         // row stride of the chunk kernel's 64 x 64 shared tables
+constexpr int kAS = kCh + 4;         // row stride of the chunk kernel's 64 x 64 D, L and X tables: 16-byte
+                                     // rows four banks apart, so a quarter-warp's 16-byte accesses to eight
+                                     // consecutive rows (or to one row) meet no bank twice
+constexpr int kY2S = 36;             // row stride of the inverse's 32 x 32 product temp (same reason)
 constexpr int kTileRows = 64;        // state rows per state-kernel CTA (the MMA M)
 constexpr int kKqBlocks = 4;         // k^ hi, lo, q^ hi, lo per (chunk, q/k head)
-constexpr int kAbHeads = 4;          // v-heads per q/k head whose gate inputs the chunk kernel prefetches
+constexpr int kAbHeads = 2;          // v-heads per q/k head whose gate inputs the chunk kernel prefetches
 
 __device__ __forceinline__ float gate_beta(float b) { return 1.f / (1.f + expf(-b)); }
 
@@ -115,23 +118,46 @@ struct ChunkLayout {
   static constexpr int YS = 2 * DK + 4;                       // row stride of the q|k conv table
   static_assert(YS % 4 == 0, "16-byte rows");
   static constexpr int Y_FLOATS = kCh * YS;
-  static constexpr int MAT = kCh * kAS;                       // one 64 x 65 matrix
+  static constexpr int MAT = kCh * kAS;                       // one 64 x 68 matrix
   static constexpr int OFF_Y = 0;                             // [64][YS]: q (0..DK-1) | k (DK..2DK-1)
   // after the Gram products, per v-head group g (two v-heads at a time): D, then X, at
   // OFF_D + 2 g MAT, and beta D (k.k) strictly lower just after it
   static constexpr int OFF_D = 0;
   static constexpr int R_FLOATS = (Y_FLOATS > 4 * MAT) ? Y_FLOATS : 4 * MAT;
-  static constexpr int OFF_KK = R_FLOATS;                     // [64][65] k^_t . k^_j
-  static constexpr int OFF_QK = OFF_KK + MAT;                 // [64][65] q^_t . k^_j
-  static constexpr int OFF_BG = OFF_QK + MAT;                 // per group: beta[64], g[64], Gamma[64]
-  static constexpr int OFF_Y2 = OFF_BG + 2 * 3 * kCh;         // per group: [32][33] product temp of the inverse
-  static constexpr int OFF_AB = OFF_Y2 + 2 * 32 * 33;         // a, b of the first kAbHeads v-heads [e][2][64]
+  static constexpr int OFF_KK = R_FLOATS;                     // [64][64] k^_t . k^_j, swizzled (gram_off)
+  static constexpr int OFF_QK = OFF_KK + kCh * kCh;           // [64][64] q^_t . k^_j, swizzled
+  static constexpr int OFF_BG = OFF_QK + kCh * kCh;           // per group: beta[64], g[64], Gamma[64]
+  static constexpr int OFF_Y2 = OFF_BG + 2 * 3 * kCh;         // per group: [32][kY2S] product temp of the inverse
+  static constexpr int OFF_AB = OFF_Y2 + 2 * 32 * kY2S;       // a, b of the first kAbHeads v-heads [e][2][64]
   static constexpr int OFF_QKD = OFF_AB + kAbHeads * 2 * kCh; // q^_t . k^_t in f32 [64]
   static constexpr int OFF_BAR = (OFF_QKD + kCh + 1) & ~1;    // 2 mbarriers, the TMEM slot
   static constexpr int FLOATS = OFF_BAR + 6;
   static_assert(4 * kCh * DK * 2 <= R_FLOATS * 4, "the split q|k operands fit in the conv table's space");
+  static_assert(MAT % 4 == 0 && OFF_KK % 4 == 0 && OFF_BG % 4 == 0 && OFF_Y2 % 4 == 0 && (32 * kY2S) % 4 == 0,
+                "16-byte aligned tables");
   static constexpr size_t BYTES = size_t(FLOATS) * 4;
+  // two CTAs per SM: each takes its bytes plus 1 KB reserved, in 128-byte units, of the SM's 228 KB
+  static_assert(2 * ((BYTES + 1024 + 127) / 128 * 128) <= 228 * 1024, "two chunk-kernel CTAs per SM");
 };
+
+// Offset of element (t, j) in the k^.k^ and q^.k^ tables: rows of 64 floats whose 16-byte groups
+// are XOR-swizzled by t mod 8, so that the row-per-thread writes from tensor memory and the
+// eight-row reads of the operand loop both spread a quarter-warp over all 32 banks.
+__device__ __forceinline__ int gram_off(int t, int j) { return t * kCh + 4 * ((j >> 2) ^ (t & 7)) + (j & 3); }
+
+// four / eight consecutive floats of shared memory at a 16-byte aligned address
+__device__ __forceinline__ void ld4(const float* src, float* v) {
+  const float4 a = *reinterpret_cast<const float4*>(src);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ __forceinline__ void ld8(const float* src, float* v) {
+  ld4(src, v);
+  ld4(src + 4, v + 4);
+}
+__device__ __forceinline__ void st8(float* dst, const float* v) {
+  *reinterpret_cast<float4*>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(dst + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
 
 template <int DK>
 __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const PrefillParams p) {
@@ -345,14 +371,16 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
         if (issued) (void)mbar_drain(sbar + 1, 0);
       }
     } else if (tid < 2 * kCh) {  // warps 0..3: thread = TMEM lane = row
-      float* dst = sm + ((tid < kCh) ? L::OFF_KK + tid * kAS : L::OFF_QK + (tid - kCh) * kAS);
+      const int row = tid & (kCh - 1);
+      float* dst = sm + ((tid < kCh) ? L::OFF_KK : L::OFF_QK);
       const uint32_t lane_sel = uint32_t(32 * (tid >> 5)) << 16;
 #pragma unroll
       for (int c0 = 0; c0 < kCh; c0 += 32) {
         float v[32];
         tmem_ld32(tmem + lane_sel + c0, v);
 #pragma unroll
-        for (int q = 0; q < 32; ++q) dst[c0 + q] = v[q];
+        for (int q = 0; q < 32; q += 4)
+          *reinterpret_cast<float4*>(dst + gram_off(row, c0 + q)) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
       }
     }
     tc_fence_before();
@@ -369,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
   float* sBeta = sm + L::OFF_BG + grp * 3 * kCh;
   float* sG = sBeta + kCh;  // g
   float* sGam = sG + kCh;
-  float* sY2 = sm + L::OFF_Y2 + grp * 32 * 33;
+  float* sY2 = sm + L::OFF_Y2 + grp * 32 * kY2S;
   for (int e0 = 0; e0 < r; e0 += 2) {
     const int e = e0 + grp;
     if (e >= r) break;  // (an odd r leaves the second half idle on the last pair)
@@ -436,16 +464,24 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
     float* gd = p.ws.gd + (size_t(c) * p.Hv + h) * (2 * kCh);
     // beta_t D (k.k) strictly below the diagonal; MQ = D (q.k) on and below it (D = 1 on the
     // diagonal, where q.k is the f32 product); Gamma, d
+    // (thread = row t, eight columns 8 jb.. 8 jb + 7: 16-byte reads and writes)
     for (int idx = gt; idx < kCh * (kCh / 8); idx += 128) {
       const int cm = idx >> 3, r8 = idx & 7;
       const int t = (cm >> 3) * 8 + r8, jb = cm & 7;
-      float v[8];
+      float d[8], kk[8], qk[8], l[8], v[8];
+      ld8(sD + t * kAS + 8 * jb, d);
+      ld4(sm + L::OFF_KK + gram_off(t, 8 * jb), kk);
+      ld4(sm + L::OFF_KK + gram_off(t, 8 * jb + 4), kk + 4);
+      ld4(sm + L::OFF_QK + gram_off(t, 8 * jb), qk);
+      ld4(sm + L::OFF_QK + gram_off(t, 8 * jb + 4), qk + 4);
+      const float bt = sBeta[t];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const int j = 8 * jb + q;
-        if (j < t) sL[t * kAS + j] = sBeta[t] * sD[t * kAS + j] * sm[L::OFF_KK + t * kAS + j];
-        v[q] = (j < t) ? sD[t * kAS + j] * sm[L::OFF_QK + t * kAS + j] : ((j == t) ? sQKd[t] : 0.f);
+        l[q] = (j < t) ? bt * d[q] * kk[q] : 0.f;
+        v[q] = (j < t) ? d[q] * qk[q] : ((j == t) ? sQKd[t] : 0.f);
       }
+      st8(sL + t * kAS + 8 * jb, l);
       uint4 hi, lo;
       split8(v, hi, lo);
       const uint32_t off = kmajor_off(t, 8 * jb, kCh);
@@ -487,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
           y0 = fmaf(l, sD[(o + k) * kAS + o + jj], y0);
           y1 = fmaf(l, sD[(o + k) * kAS + o + jj + 1], y1);
         }
-        sY2[(16 * blk + ii) * 33 + jj] = y0;
-        sY2[(16 * blk + ii) * 33 + jj + 1] = y1;
+        sY2[(16 * blk + ii) * kY2S + jj] = y0;
+        sY2[(16 * blk + ii) * kY2S + jj + 1] = y1;
       }
       gsync();
 #pragma unroll
@@ -498,46 +534,49 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_prefill_chunk_kernel(const Pr
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
           const float xv = sD[(o + 16 + ii) * kAS + o + 16 + k];
-          x0 = fmaf(xv, sY2[(16 * blk + k) * 33 + jj], x0);
-          x1 = fmaf(xv, sY2[(16 * blk + k) * 33 + jj + 1], x1);
+          x0 = fmaf(xv, sY2[(16 * blk + k) * kY2S + jj], x0);
+          x1 = fmaf(xv, sY2[(16 * blk + k) * kY2S + jj + 1], x1);
         }
         sD[(o + 16 + ii) * kAS + o + jj] = -x0;
         sD[(o + 16 + ii) * kAS + o + jj + 1] = -x1;
       }
     }
     gsync();
-    {  // the 32 x 32 off-diagonal block: thread = (row, 8 columns)
+    {  // the 32 x 32 off-diagonal block: thread = (row, 8 columns), the columns read 16 bytes at a time
       const int ii = gt >> 2, jj = 8 * (gt & 3);
       float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const float l = sL[(32 + ii) * kAS + k];
+        float xr[8];
+        ld8(sD + k * kAS + jj, xr);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) y[q] = fmaf(l, sD[k * kAS + jj + q], y[q]);
+        for (int q = 0; q < 8; ++q) y[q] = fmaf(l, xr[q], y[q]);
       }
-#pragma unroll
-      for (int q = 0; q < 8; ++q) sY2[ii * 33 + jj + q] = y[q];
+      st8(sY2 + ii * kY2S + jj, y);
       gsync();
       float x[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const float xv = sD[(32 + ii) * kAS + 32 + k];
+        float yr[8];
+        ld8(sY2 + k * kY2S + jj, yr);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) x[q] = fmaf(xv, sY2[k * 33 + jj + q], x[q]);
+        for (int q = 0; q < 8; ++q) x[q] = fmaf(xv, yr[q], x[q]);
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) sD[(32 + ii) * kAS + jj + q] = -x[q];
+      for (int q = 0; q < 8; ++q) x[q] = -x[q];
+      st8(sD + (32 + ii) * kAS + jj, x);
     }
     gsync();
     for (int idx = gt; idx < kCh * (kCh / 8); idx += 128) {
       const int cm = idx >> 3, r8 = idx & 7;
       const int t = (cm >> 3) * 8 + r8, jb = cm & 7;
-      float v[8];
+      float x[8], bj[8], v[8];
+      ld8(sD + t * kAS + 8 * jb, x);
+      ld8(sBeta + 8 * jb, bj);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const int j = 8 * jb + q;
-        v[q] = (j <= t) ? sD[t * kAS + j] * sBeta[j] : 0.f;
-      }
+      for (int q = 0; q < 8; ++q) v[q] = (8 * jb + q <= t) ? x[q] * bj[q] : 0.f;
       uint4 hi, lo;
       split8(v, hi, lo);
       const uint32_t off = kmajor_off(t, 8 * jb, kCh);
