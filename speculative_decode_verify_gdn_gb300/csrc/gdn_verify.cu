@@ -566,21 +566,49 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyPar
   // them once all CTAs got here
   griddep_launch_dependents();
 
-  // a2: L2 norm of each of the 2K vectors in place, warp per vector (rows t >= K become zero)
-  for (int n = warp; n < kNCol; n += kWarps) {
-    const int t = n % kKMax;
-    float* yr = sY + n * L::SSTRIDE;
-    float vals[DK / 32];
-    float ss = 0.f;
+  // a2: L2 norm of each of the 2K vectors in place, warp per vector; rows t >= K hold the conv's
+  // zeros and stay.  A chain window takes a warp's four vectors side by side, so that their
+  // shuffle reductions overlap (the token-tree variant, measured slower that way, one by one).
+  if constexpr (kTree) {
+    for (int n = warp; n < kNCol; n += kWarps) {
+      float* yr = sY + n * L::SSTRIDE;
+      float vals[DK / 32];
+      float ss = 0.f;
 #pragma unroll
-    for (int m = 0; m < DK / 32; ++m) {
-      vals[m] = yr[lane + 32 * m];
-      ss = fmaf(vals[m], vals[m], ss);
+      for (int m = 0; m < DK / 32; ++m) {
+        vals[m] = yr[lane + 32 * m];
+        ss = fmaf(vals[m], vals[m], ss);
+      }
+      ss = warp_sum(ss);
+      const float inv = (n % kKMax < K) ? rsqrtf(ss + p.l2_eps) : 0.f;
+#pragma unroll
+      for (int m = 0; m < DK / 32; ++m) yr[lane + 32 * m] = vals[m] * inv;
     }
-    ss = warp_sum(ss);
-    const float inv = (t < K) ? rsqrtf(ss + p.l2_eps) : 0.f;
+  } else {
+    constexpr int kPer = kNCol / kWarps;
+    static_assert(kNCol % kWarps == 0, "whole vectors per warp");
+    float vals[kPer][DK / 32], ss[kPer];
 #pragma unroll
-    for (int m = 0; m < DK / 32; ++m) yr[lane + 32 * m] = vals[m] * inv;
+    for (int u = 0; u < kPer; ++u) {
+      const int n = warp + u * kWarps;
+      ss[u] = 0.f;
+#pragma unroll
+      for (int m = 0; m < DK / 32; ++m) {
+        vals[u][m] = (n % kKMax < K) ? sY[n * L::SSTRIDE + lane + 32 * m] : 0.f;
+        ss[u] = fmaf(vals[u][m], vals[u][m], ss[u]);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) ss[u] = warp_sum(ss[u]);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int n = warp + u * kWarps;
+      if (n % kKMax < K) {
+        const float inv = rsqrtf(ss[u] + p.l2_eps);
+#pragma unroll
+        for (int m = 0; m < DK / 32; ++m) sY[n * L::SSTRIDE + lane + 32 * m] = vals[u][m] * inv;
+      }
+    }
   }
   __syncthreads();
 
