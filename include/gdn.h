@@ -122,7 +122,9 @@ gdn_status gdn_conv_step(const gdn_dims* dims, const uint16_t* x, const float* c
  * every state straight from registers) and a per-(sequence, q/k channel
  * block) kernel that writes the q|k channels' history snapshots and new
  * history once every verify CTA has read the old ones (programmatic
- * dependent launch).  The call is complete when the second kernel is.
+ * dependent launch).  The call is complete when the second kernel is.  The
+ * verify kernel is itself launched with programmatic dependent launch: it
+ * reads nothing before the kernel ahead of it on the stream has completed.
  */
 gdn_status gdn_verify_step(const gdn_dims* dims, const uint16_t* x, const uint16_t* a, const uint16_t* b,
                            const float* A_log, const float* dt_bias, const float* conv_w,

@@ -24,7 +24,9 @@
 //     (TMA) copy of its S0 tile; conv + SiLU of the 2 dk q|k channels of its q/k head (each CTA
 //     of the head computes them again: a few thousand instructions, against a table handed over
 //     between CTAs whose wait would hold back every state stream) and of its own 32 v-channels;
-//     the gates of its v-head; the L2 norms; then the recurrence.
+//     the gates of its v-head; the L2 norms; then the recurrence.  Launched with programmatic
+//     dependent launch (its CTAs may be scheduled while the kernel ahead of it finishes; they
+//     wait for it before reading anything).
 //  2. qk_history: the K history snapshots and the new history of the q|k channels, which all
 //     CTAs of a q/k head read and so none of them may rewrite in place.  Launched with
 //     programmatic dependent launch: it can start only once every verify CTA has passed the
@@ -372,6 +374,9 @@ __device__ __forceinline__ void reduce4_pair(const float (&p)[4], const float (&
 // t, [win[t+1], win[t+2], x_t]; of a token tree, the history after node t along its path.
 template <bool kTree>
 __global__ void __launch_bounds__(kHistThreads) gdn_qk_history_kernel(const VerifyParams p) {
+  // the next call's verify CTAs may be scheduled from here on: each waits for this grid's
+  // completion, which follows the verify grid's, before it reads anything
+  griddep_launch_dependents();
   __shared__ TreeTable tree_s;
   __shared__ float2 sx[kTree ? kKMax * kHistThreads : 1];
   const int b = blockIdx.y;
@@ -492,6 +497,10 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyPar
   const int r0 = (blockIdx.x % kTiles) * kRows;
   const int kh = h / (p.Hv / p.Hk);
   const size_t tile_off = ((size_t(b) * p.Hv + h) * DV + r0) * DK;
+  // Launched with programmatic dependent launch, the CTA may start while the kernel before it on
+  // the stream still runs: nothing is read from global memory before this wait, which returns
+  // once that kernel has completed and its writes are visible.
+  griddep_wait();
 
   // gated: the partial sums of o^2 of all kTiles CTAs of the head land on bar_sq (8 bytes from
   // each of 8 lanes of every warp of every CTA, own included)
@@ -892,15 +901,19 @@ cudaError_t launch_t(const VerifyParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = b1;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  // programmatic dependent launch: the CTAs may be scheduled while the previous kernel on the
+  // stream finishes (they wait for it before any global read)
+  cudaLaunchAttribute attr[2];
   cfg.attrs = attr;
-  cfg.numAttrs = 0;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.numAttrs = 1;
   if constexpr (kGated) {  // the row tiles of one v-head form a cluster (they share the output norm)
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = DV / kRows;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = DV / kRows;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   e = cudaLaunchKernelEx(&cfg, k1, p);
   if (e != cudaSuccess) return e;
