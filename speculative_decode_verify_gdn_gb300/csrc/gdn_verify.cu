@@ -754,8 +754,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_verify_kernel(const VerifyPar
       // partial), so that the two butterflies' shuffles hide each other's latency on the path
       // from one token to the next; the sums are the same, added in the same order.  Measured
       // against reducing o in its own token: resume step 190.9 -> 189.6 us, B = 32 K = 8 rounds
-      // 106.1 -> 102.0 us, 48-layer stack 2.72 -> 2.58 ms; graph-replayed decode 4.62 -> 4.87 us
-      // (skipping the first token's zero shuffles lost on every shape and did not change decode)
+      // 106.1 -> 102.0 us, 48-layer stack 2.72 -> 2.58 ms (a run-time skip of the first token's
+      // zero shuffles lost on every shape; plain decode has its own K = 1 instantiation, with
+      // no overlap to make)
       float op = 0.f;
       auto keep_o = [&](int tt, float ov) {
         ov *= p.q_scale;
