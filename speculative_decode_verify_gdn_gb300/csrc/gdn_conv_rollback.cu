@@ -11,7 +11,9 @@
 // commits on snapshot rollback and device-resident checkpoints; atlas #297, per-token
 // conv_state intermediates for partial-accept rollback).  The source is the verify step's
 // intermediate after token L-1, or the pre-window snapshot for L = 0; L = K needs no copy.
-// The copy is a streaming float4 copy: each thread keeps eight 16-byte loads in flight.
+// The copy is a streaming float4 copy: each thread keeps eight 16-byte loads in flight.  It is
+// launched with programmatic dependent launch, as the verify kernel is: its CTAs may be
+// scheduled while the kernel ahead of it finishes, and the next verify call's while it runs.
 #include "gdn_common.cuh"
 #include "gdn_kernels.h"
 
@@ -67,6 +69,10 @@ __device__ __forceinline__ float4 ld_stream(const float4* p) {
 
 // grid.x: state chunks then conv chunks of one sequence; grid.y: sequence.
 __global__ void __launch_bounds__(kRbThreads) gdn_rollback_kernel(const RollbackParams p, int state_chunks) {
+  // the next kernel on the stream may be scheduled from here on (a verify kernel waits for this
+  // grid before it reads anything); this one reads nothing before the kernel ahead of it is done
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int b = blockIdx.y;
   const int L = p.accept_len[b];
   if (L < 0 || L > p.K) {
@@ -117,9 +123,17 @@ cudaError_t launch_conv(const ConvParams& p, cudaStream_t stream) {
 cudaError_t launch_rollback(const RollbackParams& p, cudaStream_t stream) {
   const int state_chunks = int((p.state_elems + kRbChunk - 1) / kRbChunk);
   const int conv_chunks = int((p.conv_elems + kRbChunk - 1) / kRbChunk);
-  dim3 grid(unsigned(state_chunks + conv_chunks), unsigned(p.B), 1);
-  gdn_rollback_kernel<<<grid, kRbThreads, 0, stream>>>(p, state_chunks);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(state_chunks + conv_chunks), unsigned(p.B), 1);
+  cfg.blockDim = dim3(kRbThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gdn_rollback_kernel, p, state_chunks);
 }
 
 }  // namespace gdn
