@@ -141,3 +141,37 @@ def test_graph_replay_equals_eager():
     assert torch.equal(st.conv_state, ref.conv_state)
     assert torch.equal(st.out, ref.out)
     assert torch.equal(st.state_inter, ref.state_inter)
+
+
+def test_verify_right_after_prefill():
+    """A prefill writes the state and conv history in place and a verify window reads them,
+    launched right after it with no synchronisation (the prefill's last kernel does not signal
+    its dependents early, so the verify kernel waits for its completion): the same results, bit
+    for bit, as with a synchronisation in between."""
+    from speculative_decode_verify_gdn_gb300.synth import make_prompts
+
+    d = Dims(B=3, K=12, Hk=2, Hv=4, dk=128, dv=128)
+    g = Gen(4700)
+    lay = make_layer(g, d, Dists())
+    pr = make_prompts(g, d, [200, 77, 130], Dists())
+    rnd = make_round(g, d, Dists())
+    pdims = gdn.make_dims(d.B, 1, d.Hk, d.Hv, d.dk, d.dv, d.W, 1.0, 1e-6, 1)
+    N = int(pr.x.shape[0])
+    bf = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+    cu, px, pa, pb = torch.from_numpy(pr.cu).cuda(), bf(pr.x), bf(pr.a), bf(pr.b)
+    pout = torch.empty((N, d.Hv, d.dv), dtype=torch.float32, device="cuda")
+    pws = gdn.alloc_prefill_workspace(pdims, N)
+    results = []
+    for sync in (True, False):
+        st = GdnLayerState.create(d, lay)
+        st.load_round(rnd)
+        torch.cuda.synchronize()
+        gdn.gdn_prefill(pdims, cu, px, pa, pb, st.A_log, st.dt_bias, st.conv_w, st.conv_states[0], st.conv_states[0],
+                        st.states[0], st.states[0], pout, pws)
+        if sync:
+            torch.cuda.synchronize()
+        st.verify()
+        torch.cuda.synchronize()
+        results.append([t.clone() for t in (st.out, st.states[0], st.state_inter, st.conv_states[0], st.conv_inter)])
+    for a, b in zip(*results):
+        assert torch.equal(a, b)
